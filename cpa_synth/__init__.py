@@ -1,0 +1,283 @@
+"""Seeded synthetic workloads for cascade verify and prefix-hit prefill.
+
+This module only *makes inputs*: random bf16 tensors, page tables and
+sequence lengths.  It holds none of the attention arithmetic, so both the
+fp64 oracle (``oracle/``) and the CUDA path (``cascade_paged_attention_gb300``)
+can consume the same bits without sharing any of the method's code.
+
+Layout conventions written here (the reader side lives separately in the
+oracle's C code and in the CUDA kernels):
+
+* K/V page pool: ``[num_pages, page_size, H_kv, head_dim]`` bf16 (stored as
+  uint16 bit patterns).  Logical position ``pos`` of a sequence lives in page
+  ``table[pos // page_size]`` at slot ``pos % page_size`` (the block-table rule
+  of the KV-cache tutorial, "PagedAttention" section, ``append_token``).
+* Queries ``q``: ``[T, H_q, head_dim]``; for verify, token
+  ``t = (b * topk + k) * S + s`` is draft token ``s`` of branch ``k`` of
+  request ``b``.
+* Page tables are int32, padded with -1 past each row's used pages.
+
+Values are N(0, 1) fp32 rounded to bf16 (round-to-nearest-even).  Slots of a
+page that lie past a sequence's end are filled with ``pad_fill`` ("random" or
+"nan") so that a reader which touches them shows up in the results.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+
+__all__ = [
+    "build_pool",
+    "table_matrix",
+    "VerifyWorkload",
+    "PrefillWorkload",
+    "make_verify",
+    "make_prefill",
+    "VERIFY_CONFIGS",
+    "PREFILL_CONFIG",
+    "bf16_bits_from_f32",
+    "f32_from_bf16_bits",
+]
+
+
+def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (nearest-even) and return the uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounding = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((u + rounding) >> np.uint32(16)).astype(np.uint16)
+
+
+def f32_from_bf16_bits(b: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to fp32 (exact)."""
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+_NAN_BF16 = np.uint16(0x7FC0)
+
+
+def _normal_bf16(rng: np.random.Generator, shape) -> np.ndarray:
+    n = int(np.prod(shape)) if len(shape) else 1
+    out = np.empty(n, dtype=np.uint16)
+    chunk = 1 << 24
+    for lo in range(0, n, chunk):
+        hi = min(n, lo + chunk)
+        out[lo:hi] = bf16_bits_from_f32(rng.standard_normal(hi - lo, dtype=np.float32))
+    return out.reshape(shape)
+
+
+@dataclasses.dataclass
+class VerifyWorkload:
+    """Inputs of one verify step (one layer): B requests, topk chain branches of S drafts."""
+
+    B: int
+    topk: int
+    S: int
+    H_q: int
+    H_kv: int
+    head_dim: int
+    page_size: int
+    prefix_lens: np.ndarray          # int32 [B]
+    q: np.ndarray                    # uint16 [B*topk*S, H_q, d]
+    k_pages: np.ndarray              # uint16 [num_pages, P, H_kv, d]
+    v_pages: np.ndarray              # uint16 [num_pages, P, H_kv, d]
+    prefix_page_table: np.ndarray    # int32 [B, max_prefix_pages]
+    draft_page_table: np.ndarray     # int32 [B*topk, max_draft_pages]
+    max_prefix_len: int
+    # Logical (de-paged) K/V, only when requested: lists indexed by request /
+    # virtual request, each uint16 [len, H_kv, d].
+    prefix_k: Optional[list] = None
+    prefix_v: Optional[list] = None
+    draft_k: Optional[list] = None
+    draft_v: Optional[list] = None
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_pages.shape[0])
+
+    @property
+    def n_tokens(self) -> int:
+        return self.B * self.topk * self.S
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    def unique_kv_tokens(self) -> int:
+        """Prefix tokens once per request plus every branch's own drafts."""
+        return int(self.prefix_lens.astype(np.int64).sum()) + self.B * self.topk * self.S
+
+    def naive_kv_tokens(self) -> int:
+        """Every virtual request (b, k) re-reads its request's prefix plus its drafts."""
+        return int(self.topk * (self.prefix_lens.astype(np.int64) + self.S).sum())
+
+    def kv_bytes_per_token(self) -> int:
+        return 2 * self.H_kv * self.head_dim * 2
+
+
+@dataclasses.dataclass
+class PrefillWorkload:
+    """Inputs of a prefill after a prefix-cache hit of H tokens (same N for every request)."""
+
+    B: int
+    N: int
+    H: int
+    H_q: int
+    H_kv: int
+    head_dim: int
+    page_size: int
+    q: np.ndarray           # uint16 [B*M, H_q, d] suffix queries, M = N - H
+    k_pages: np.ndarray     # uint16 [num_pages, P, H_kv, d]
+    v_pages: np.ndarray
+    page_table: np.ndarray  # int32 [B, ceil(N/P)]
+    seq_k: Optional[list] = None  # logical K per request [N, H_kv, d] (optional)
+    seq_v: Optional[list] = None
+
+    @property
+    def M(self) -> int:
+        return self.N - self.H
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_pages.shape[0])
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    def visible_pairs(self) -> int:
+        """Query-key pairs the suffix must still compute, per request and q head."""
+        N, H = self.N, self.H
+        return (N * (N + 1) - H * (H + 1)) // 2
+
+
+def build_pool(k_seqs, v_seqs, page_size: int, perm_rng: np.random.Generator,
+               pad_fill: str = "random", spare_pages: int = 0):
+    """Page a list of logical sequences into one K pool and one V pool.
+
+    ``k_seqs[i]`` / ``v_seqs[i]`` are uint16 ``[len_i, H_kv, d]``.  Each
+    sequence gets ``ceil(len_i / page_size)`` physical pages drawn from one
+    random permutation of the pool; token ``pos`` goes to page
+    ``table_i[pos // page_size]``, slot ``pos % page_size``.  Returns
+    ``(k_pages, v_pages, tables)`` with ``tables[i]`` an int32 array.
+    """
+    assert len(k_seqs) == len(v_seqs)
+    P = page_size
+    if k_seqs:
+        H_kv, d = k_seqs[0].shape[1], k_seqs[0].shape[2]
+    else:
+        H_kv, d = 1, 1
+    counts = [(int(x.shape[0]) + P - 1) // P for x in k_seqs]
+    total = int(sum(counts)) + spare_pages
+    perm = perm_rng.permutation(total).astype(np.int32)
+    shape = (total, P, H_kv, d)
+    if pad_fill == "nan":
+        k_pages = np.full(shape, _NAN_BF16, dtype=np.uint16)
+        v_pages = np.full(shape, _NAN_BF16, dtype=np.uint16)
+    elif pad_fill == "random":
+        k_pages = _normal_bf16(perm_rng, shape)
+        v_pages = _normal_bf16(perm_rng, shape)
+    elif pad_fill == "zero":
+        k_pages = np.zeros(shape, dtype=np.uint16)
+        v_pages = np.zeros(shape, dtype=np.uint16)
+    else:
+        raise ValueError(pad_fill)
+    tables = []
+    cur = 0
+    for ks, vs, n in zip(k_seqs, v_seqs, counts):
+        tab = perm[cur:cur + n].copy()
+        cur += n
+        pos = np.arange(ks.shape[0])
+        if pos.size:
+            k_pages[tab[pos // P], pos % P] = ks
+            v_pages[tab[pos // P], pos % P] = vs
+        tables.append(tab)
+    return k_pages, v_pages, tables
+
+
+def table_matrix(tables, width: int) -> np.ndarray:
+    """Stack per-sequence page lists into an int32 matrix padded with -1."""
+    out = np.full((len(tables), max(1, width)), -1, dtype=np.int32)
+    for i, t in enumerate(tables):
+        out[i, :len(t)] = t
+    return out
+
+
+def make_verify(B: int, topk: int, S: int, H_q: int, H_kv: int, head_dim: int = 128,
+                page_size: int = 16, L: Optional[int] = None,
+                L_range: Optional[tuple[int, int]] = None, prefix_lens=None,
+                seed: int = 0, perm_seed: Optional[int] = None, pad_fill: str = "random",
+                spare_pages: int = 0, keep_logical: bool = False) -> VerifyWorkload:
+    """Build one verify workload.
+
+    The logical contents (q, every sequence's K/V) depend only on ``seed``;
+    the physical placement of pages depends only on ``perm_seed``, so two
+    workloads that differ in ``perm_seed`` hold the same logical data.
+    """
+    rng = np.random.default_rng(seed)
+    if prefix_lens is not None:
+        lens = np.asarray(prefix_lens, dtype=np.int32).copy()
+        assert lens.shape == (B,)
+    elif L_range is not None:
+        lens = rng.integers(L_range[0], L_range[1] + 1, size=B).astype(np.int32)
+    else:
+        assert L is not None
+        lens = np.full(B, L, dtype=np.int32)
+    P = page_size
+    d = head_dim
+    T = B * topk * S
+    q = _normal_bf16(rng, (T, H_q, d))
+    pk = [_normal_bf16(rng, (int(lens[b]), H_kv, d)) for b in range(B)]
+    pv = [_normal_bf16(rng, (int(lens[b]), H_kv, d)) for b in range(B)]
+    dk = [_normal_bf16(rng, (S, H_kv, d)) for _ in range(B * topk)]
+    dv = [_normal_bf16(rng, (S, H_kv, d)) for _ in range(B * topk)]
+
+    perm_rng = np.random.default_rng(seed * 7919 + 17 if perm_seed is None else perm_seed)
+    k_pages, v_pages, tables = build_pool(pk + dk, pv + dv, P, perm_rng, pad_fill, spare_pages)
+    max_prefix_len = int(lens.max()) if B > 0 else 0
+    prefix_pt = table_matrix(tables[:B], (max_prefix_len + P - 1) // P)
+    draft_pt = table_matrix(tables[B:], (S + P - 1) // P)
+
+    wl = VerifyWorkload(B=B, topk=topk, S=S, H_q=H_q, H_kv=H_kv, head_dim=d, page_size=P,
+                        prefix_lens=lens, q=q, k_pages=k_pages, v_pages=v_pages,
+                        prefix_page_table=prefix_pt, draft_page_table=draft_pt,
+                        max_prefix_len=max_prefix_len)
+    if keep_logical:
+        wl.prefix_k, wl.prefix_v, wl.draft_k, wl.draft_v = pk, pv, dk, dv
+    return wl
+
+
+def make_prefill(B: int, N: int, H: int, H_q: int, H_kv: int, head_dim: int = 128,
+                 page_size: int = 16, seed: int = 0, perm_seed: Optional[int] = None,
+                 pad_fill: str = "random", keep_logical: bool = False) -> PrefillWorkload:
+    """Build one prefix-hit prefill workload: every request has N tokens, the first H cached."""
+    assert 0 <= H <= N
+    rng = np.random.default_rng(seed)
+    P = page_size
+    d = head_dim
+    M = N - H
+    q = _normal_bf16(rng, (B * M, H_q, d))
+    sk = [_normal_bf16(rng, (N, H_kv, d)) for _ in range(B)]
+    sv = [_normal_bf16(rng, (N, H_kv, d)) for _ in range(B)]
+    perm_rng = np.random.default_rng(seed * 7919 + 17 if perm_seed is None else perm_seed)
+    k_pages, v_pages, tables = build_pool(sk, sv, P, perm_rng, pad_fill)
+    pt = table_matrix(tables, (N + P - 1) // P)
+    wl = PrefillWorkload(B=B, N=N, H=H, H_q=H_q, H_kv=H_kv, head_dim=d, page_size=P, q=q,
+                         k_pages=k_pages, v_pages=v_pages, page_table=pt)
+    if keep_logical:
+        wl.seq_k, wl.seq_v = sk, sv
+    return wl
+
+
+# The five workloads the method is exercised on, by name.  Verify shapes come
+# from the pages' example (L=2000, topk=4, S=5) and its neighbours.
+VERIFY_CONFIGS = {
+    "tiny": dict(B=2, topk=2, S=3, L=64, H_q=8, H_kv=2, page_size=16, seed=1),
+    "llama3_8b": dict(B=32, topk=4, S=3, L=1000, H_q=32, H_kv=8, page_size=16, seed=2),
+    "pages_example": dict(B=64, topk=4, S=5, L=2000, H_q=32, H_kv=8, page_size=16, seed=3),
+    "long_variable": dict(B=16, topk=8, S=4, L_range=(1024, 32768), H_q=64, H_kv=8,
+                          page_size=64, seed=4),
+}
+PREFILL_CONFIG = dict(B=8, N=8192, H_q=32, H_kv=8, page_size=16, seed=5, hits=(0.0, 0.5, 0.75))
