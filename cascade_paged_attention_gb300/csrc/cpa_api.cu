@@ -1,0 +1,489 @@
+// cpa_api.cu -- the extern "C" entry points of libcpa.so: argument checks,
+// TMA tensor maps, workspace layout and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "cpa.h"
+#include "cpa_attn.cuh"
+#include "cpa_small.h"
+
+namespace cpa {
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+constexpr int kMaxSmemOptin = 232448;  // 227 KB per CTA on sm_100-class parts
+
+// ---------------------------------------------------------------- device facts
+int smem_optin() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+// ---------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// bf16 tensor [dim2][dim1][128] seen as (d, dim1, dim2), 128-B swizzled boxes
+// of {64, box1, box2}.
+bool make_map(CUtensorMap* map, const void* base, uint64_t dim1, uint64_t dim2, uint32_t box1,
+              uint32_t box2) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128, dim1, dim2};
+    cuuint64_t strides[2] = {128 * 2, dim1 * 128 * 2};
+    cuuint32_t box[3] = {64, box1, box2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+bool page_size_ok(int P) { return P >= 8 && P <= 256 && pow2(P); }
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- workspace layout
+struct WsLayout {
+    size_t counters, part_lse, part_o, total;
+};
+WsLayout ws_layout(long long n_units, int n_sm) {
+    WsLayout w;
+    w.counters = kStatusBytes;
+    w.part_lse = align_up(w.counters + (size_t)n_units * 4, 256);
+    w.part_o = align_up(w.part_lse + (size_t)2 * n_sm * kMaxUnitRows * 4, 256);
+    w.total = align_up(w.part_o + (size_t)2 * n_sm * kMaxUnitRows * 128 * 4, 256);
+    return w;
+}
+
+// ---------------------------------------------------------------- launch config
+struct Geometry {
+    int num_mt;
+    int TS, TSB, Rq;
+    int n_stages, n_qbufs;
+    uint32_t off_q, off_kv, off_p, off_draft;
+    int smem_bytes;
+};
+
+bool plan_geometry(int G, int TS, bool draft, bool prefill, Geometry& g) {
+    const int rows = TS * G;
+    if (rows <= 0 || rows > kMaxUnitRows) return false;
+    g.num_mt = rows <= 128 ? 1 : 2;
+    g.TS = TS;
+    g.TSB = g.num_mt == 1 ? TS : 128 / G;
+    const int rows_mt = G * g.TSB;
+    if (rows_mt > 128) return false;
+    g.Rq = (rows_mt + 7) / 8 * 8;
+    const int pbufs = g.num_mt == 1 ? 2 : 1;
+    const size_t qmt = (size_t)2 * g.Rq * 128;
+    const int tries[5][2] = {{4, 2}, {4, 1}, {3, 2}, {3, 1}, {2, 1}};
+    for (int t = 0; t < 5; ++t) {
+        int st = tries[t][0], qb = tries[t][1];
+        if (g.num_mt == 2 && qb == 2) continue;
+        if (prefill && st == 4 && qb == 2) continue;  // prefer Q double-buffering at 3 stages
+        size_t off_q = kOffData;
+        size_t off_kv = align_up(off_q + (size_t)qb * g.num_mt * qmt, 1024);
+        size_t off_p = off_kv + (size_t)st * kStageBytes;
+        size_t off_d = off_p + (size_t)g.num_mt * pbufs * kPBytes;
+        size_t end = off_d + (draft ? (size_t)kMaxDraftKeys * 512 : 0);
+        size_t total = end + 1024;
+        if (total <= (size_t)kMaxSmemOptin) {
+            g.n_stages = st;
+            g.n_qbufs = qb;
+            g.off_q = (uint32_t)off_q;
+            g.off_kv = (uint32_t)off_kv;
+            g.off_p = (uint32_t)off_p;
+            g.off_draft = (uint32_t)off_d;
+            g.smem_bytes = (int)total;
+            return true;
+        }
+    }
+    return false;
+}
+
+template <int NUM_MT>
+cudaError_t launch_attn(const AttnParams& p, int smem, int grid, cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        const int optin = smem_optin();
+        attr_err = cudaFuncSetAttribute(paged_attn_kernel<NUM_MT>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        optin < kMaxSmemOptin ? optin : kMaxSmemOptin);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    if (smem > smem_optin()) return cudaErrorInvalidValue;
+    paged_attn_kernel<NUM_MT><<<grid, Cfg<NUM_MT>::kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cpa_status run_attn(AttnParams& p, const Geometry& geo, long long n_units, void* workspace,
+                    size_t ws_bytes, cudaStream_t stream) {
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return CPA_ERR_CUDA;
+    const WsLayout wl = ws_layout(n_units, n_sm);
+    if (!workspace) return CPA_ERR_WORKSPACE;
+    if (ws_bytes < wl.total) return CPA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CPA_ERR_INVALID_ARG;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.status = reinterpret_cast<uint32_t*>(ws);
+    p.counters = reinterpret_cast<uint32_t*>(ws + wl.counters);
+    p.part_lse = reinterpret_cast<float*>(ws + wl.part_lse);
+    p.part_o = reinterpret_cast<float*>(ws + wl.part_o);
+    p.TS = geo.TS;
+    p.TSB = geo.TSB;
+    p.Rq = geo.Rq;
+    p.n_stages = geo.n_stages;
+    p.n_qbufs = geo.n_qbufs;
+    p.off_q = geo.off_q;
+    p.off_kv = geo.off_kv;
+    p.off_p = geo.off_p;
+    p.off_draft = geo.off_draft;
+    if (cudaMemsetAsync(workspace, 0, wl.part_lse, stream) != cudaSuccess) return CPA_ERR_CUDA;
+    cudaError_t e = geo.num_mt == 1 ? launch_attn<1>(p, geo.smem_bytes, n_sm, stream)
+                                    : launch_attn<2>(p, geo.smem_bytes, n_sm, stream);
+    return e == cudaSuccess ? CPA_OK : CPA_ERR_LAUNCH;
+}
+
+// Checks shared by the verify entry points.
+cpa_status check_verify(const void* q, const void* k_pages, const void* v_pages,
+                        const int32_t* ppt, int ppt_stride, const int32_t* lens, int B, int topk,
+                        int S, int H_q, int H_kv, int head_dim, int page_size, int num_pages,
+                        int max_prefix_len, float sm_scale) {
+    if (!q || !k_pages || !v_pages || !ppt || !lens) return CPA_ERR_INVALID_ARG;
+    if (B < 1 || topk < 1 || S < 1 || H_q < 1 || H_kv < 1 || num_pages < 1 || max_prefix_len < 0)
+        return CPA_ERR_INVALID_ARG;
+    if (H_q % H_kv != 0) return CPA_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale)) return CPA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages)) return CPA_ERR_INVALID_ARG;
+    if (head_dim != 128) return CPA_ERR_UNSUPPORTED;
+    if (!page_size_ok(page_size)) return CPA_ERR_UNSUPPORTED;
+    const int G = H_q / H_kv;
+    if (!pow2(G) || G > 128) return CPA_ERR_UNSUPPORTED;
+    const long long need_pages = ((long long)max_prefix_len + page_size - 1) / page_size;
+    if (ppt_stride < 1 || ppt_stride < need_pages) return CPA_ERR_INVALID_ARG;
+    if ((long long)num_pages * page_size > (1ll << 31)) return CPA_ERR_UNSUPPORTED;
+    if ((long long)B * topk * S * H_q > (1ll << 31) / 128) return CPA_ERR_UNSUPPORTED;
+    return CPA_OK;
+}
+
+void fill_common(AttnParams& p, const void* q, const void* k_pages, const void* v_pages,
+                 const int32_t* ppt, int ppt_stride, const int32_t* dpt, int dpt_stride,
+                 const int32_t* lens, int B, int topk, int S, int H_q, int H_kv, int page_size,
+                 int num_pages, int max_prefix_len, float sm_scale) {
+    std::memset(&p, 0, sizeof p);
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
+    p.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
+    p.ptab = ppt;
+    p.ptab_stride = ppt_stride;
+    p.dtab = dpt;
+    p.dtab_stride = dpt_stride;
+    p.lens = lens;
+    p.B = B;
+    p.topk = topk;
+    p.S = S;
+    p.H_q = H_q;
+    p.H_kv = H_kv;
+    p.G = H_q / H_kv;
+    p.P = page_size;
+    p.num_pages = num_pages;
+    p.max_len = max_prefix_len;
+    p.boxr = page_size < kBN ? page_size : kBN;
+    p.scale_log2 = sm_scale * kLog2e;
+}
+
+bool kv_maps(AttnParams& p, const void* k_pages, const void* v_pages, int H_kv, int num_pages,
+             int page_size) {
+    const uint64_t rows = (uint64_t)num_pages * page_size;
+    return make_map(&p.kmap, k_pages, H_kv, rows, 1, p.boxr) &&
+           make_map(&p.vmap, v_pages, H_kv, rows, 1, p.boxr);
+}
+
+cpa_status verify_common(int mode, const void* q, const void* k_pages, const void* v_pages,
+                         const int32_t* ppt, int ppt_stride, const int32_t* dpt, int dpt_stride,
+                         const int32_t* lens, int B, int topk, int S, int H_q, int H_kv,
+                         int head_dim, int page_size, int num_pages, int max_prefix_len,
+                         float sm_scale, void* o, float* lse, void* workspace, size_t ws_bytes,
+                         cudaStream_t stream) {
+    cpa_status st = check_verify(q, k_pages, v_pages, ppt, ppt_stride, lens, B, topk, S, H_q, H_kv,
+                                 head_dim, page_size, num_pages, max_prefix_len, sm_scale);
+    if (st != CPA_OK) return st;
+    if (!o || !lse || !aligned16(o)) return CPA_ERR_INVALID_ARG;
+    const bool draft = mode != MODE_PASS_A;
+    if (draft) {
+        if (!dpt || dpt_stride < (S + page_size - 1) / page_size) return CPA_ERR_INVALID_ARG;
+        if (S > kMaxDraft) return CPA_ERR_UNSUPPORTED;
+    }
+    const int G = H_q / H_kv;
+    const int TS = mode == MODE_NAIVE ? S : topk * S;
+    if (draft && TS > kMaxDraftKeys) return CPA_ERR_UNSUPPORTED;
+    Geometry geo;
+    if (!plan_geometry(G, TS, draft, false, geo)) return CPA_ERR_UNSUPPORTED;
+    AttnParams p;
+    fill_common(p, q, k_pages, v_pages, ppt, ppt_stride, dpt, dpt_stride, lens, B, topk, S, H_q,
+                H_kv, page_size, num_pages, max_prefix_len, sm_scale);
+    p.mode = mode;
+    p.upg = mode == MODE_NAIVE ? topk * H_kv : H_kv;
+    p.draft_keys = draft ? TS : 0;
+    p.o = o;
+    p.lse = lse;
+    const uint64_t T = (uint64_t)B * topk * S;
+    if (!make_map(&p.qmap, q, H_q, T, G, geo.TSB)) return CPA_ERR_CUDA;
+    if (!kv_maps(p, k_pages, v_pages, H_kv, num_pages, page_size)) return CPA_ERR_CUDA;
+    const long long n_units = (long long)B * p.upg;
+    return run_attn(p, geo, n_units, workspace, ws_bytes, stream);
+}
+
+}  // namespace
+}  // namespace cpa
+
+using namespace cpa;
+
+extern "C" {
+
+const char* cpa_status_string(cpa_status s) {
+    switch (s) {
+        case CPA_OK: return "ok";
+        case CPA_ERR_INVALID_ARG: return "invalid argument";
+        case CPA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case CPA_ERR_WORKSPACE: return "workspace missing or too small";
+        case CPA_ERR_LAUNCH: return "kernel launch failed";
+        case CPA_ERR_BAD_PAGE: return "page id out of range";
+        case CPA_ERR_TIMEOUT: return "device wait timed out";
+        case CPA_ERR_CUDA: return "CUDA runtime error";
+        case CPA_ERR_BAD_LENGTH: return "prefix length out of range";
+    }
+    return "unknown status";
+}
+
+int cpa_version(void) { return 100; }
+
+size_t cpa_status_workspace_size(void) { return kStatusBytes; }
+
+size_t cpa_cascade_verify_workspace_size(int B, int topk, int S, int H_q, int H_kv, int head_dim,
+                                         int page_size) {
+    if (B < 1 || topk < 1 || S < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv || head_dim != 128 ||
+        !page_size_ok(page_size))
+        return 0;
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return 0;
+    return ws_layout((long long)B * topk * H_kv, n_sm).total;
+}
+
+cpa_status cpa_cascade_verify(const void* q, const void* k_pages, const void* v_pages,
+                              const int32_t* prefix_page_table, int prefix_pt_stride,
+                              const int32_t* draft_page_table, int draft_pt_stride,
+                              const int32_t* prefix_lens, int B, int topk, int S, int H_q,
+                              int H_kv, int head_dim, int page_size, int num_pages,
+                              int max_prefix_len, float sm_scale, void* o, float* lse,
+                              void* workspace, size_t workspace_bytes, cpa_stream_t stream) {
+    return verify_common(MODE_CASCADE, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                         draft_page_table, draft_pt_stride, prefix_lens, B, topk, S, H_q, H_kv,
+                         head_dim, page_size, num_pages, max_prefix_len, sm_scale, o, lse,
+                         workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+cpa_status cpa_naive_expand_verify(const void* q, const void* k_pages, const void* v_pages,
+                                   const int32_t* prefix_page_table, int prefix_pt_stride,
+                                   const int32_t* draft_page_table, int draft_pt_stride,
+                                   const int32_t* prefix_lens, int B, int topk, int S, int H_q,
+                                   int H_kv, int head_dim, int page_size, int num_pages,
+                                   int max_prefix_len, float sm_scale, void* o, float* lse,
+                                   void* workspace, size_t workspace_bytes, cpa_stream_t stream) {
+    return verify_common(MODE_NAIVE, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                         draft_page_table, draft_pt_stride, prefix_lens, B, topk, S, H_q, H_kv,
+                         head_dim, page_size, num_pages, max_prefix_len, sm_scale, o, lse,
+                         workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+cpa_status cpa_cascade_pass_a(const void* q, const void* k_pages, const void* v_pages,
+                              const int32_t* prefix_page_table, int prefix_pt_stride,
+                              const int32_t* prefix_lens, int B, int topk, int S, int H_q,
+                              int H_kv, int head_dim, int page_size, int num_pages,
+                              int max_prefix_len, float sm_scale, float* o_a, float* lse_a,
+                              void* workspace, size_t workspace_bytes, cpa_stream_t stream) {
+    return verify_common(MODE_PASS_A, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                         nullptr, 0, prefix_lens, B, topk, S, H_q, H_kv, head_dim, page_size,
+                         num_pages, max_prefix_len, sm_scale, o_a, lse_a, workspace,
+                         workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+cpa_status cpa_cascade_pass_b(const void* q, const void* k_pages, const void* v_pages,
+                              const int32_t* draft_page_table, int draft_pt_stride, int B,
+                              int topk, int S, int H_q, int H_kv, int head_dim, int page_size,
+                              int num_pages, float sm_scale, float* o_b, float* lse_b,
+                              void* workspace, size_t workspace_bytes, cpa_stream_t stream) {
+    if (!q || !k_pages || !v_pages || !draft_page_table || !o_b || !lse_b)
+        return CPA_ERR_INVALID_ARG;
+    if (B < 1 || topk < 1 || S < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv || num_pages < 1 ||
+        page_size < 1 || !std::isfinite(sm_scale))
+        return CPA_ERR_INVALID_ARG;
+    if (head_dim != 128) return CPA_ERR_UNSUPPORTED;
+    if (draft_pt_stride < (S + page_size - 1) / page_size) return CPA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) & 7u) || (reinterpret_cast<uintptr_t>(k_pages) & 7u) ||
+        (reinterpret_cast<uintptr_t>(v_pages) & 7u) || !aligned16(o_b))
+        return CPA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kStatusBytes) return CPA_ERR_WORKSPACE;
+    PassBParams p;
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
+    p.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
+    p.dtab = draft_page_table;
+    p.dtab_stride = draft_pt_stride;
+    p.B = B;
+    p.topk = topk;
+    p.S = S;
+    p.H_q = H_q;
+    p.H_kv = H_kv;
+    p.P = page_size;
+    p.num_pages = num_pages;
+    p.scale_log2 = sm_scale * kLog2e;
+    p.o_b = o_b;
+    p.lse_b = lse_b;
+    p.status = static_cast<uint32_t*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(workspace, 0, kStatusBytes, s) != cudaSuccess) return CPA_ERR_CUDA;
+    return launch_pass_b(p, s) == cudaSuccess ? CPA_OK : CPA_ERR_LAUNCH;
+}
+
+cpa_status cpa_merge_state(const float* o_a, const float* lse_a, const float* o_b,
+                           const float* lse_b, int n_tokens, int H, int head_dim, void* o_out,
+                           float* lse_out, cpa_stream_t stream) {
+    if (!o_a || !lse_a || !o_b || !lse_b || !o_out || !lse_out) return CPA_ERR_INVALID_ARG;
+    if (n_tokens < 0 || H < 1 || head_dim < 4 || head_dim % 4 != 0) return CPA_ERR_INVALID_ARG;
+    if (head_dim > 512) return CPA_ERR_UNSUPPORTED;
+    if (!aligned16(o_a) || !aligned16(o_b) || (reinterpret_cast<uintptr_t>(o_out) & 7u))
+        return CPA_ERR_INVALID_ARG;
+    const long long rows = (long long)n_tokens * H;
+    if (rows == 0) return CPA_OK;
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return CPA_ERR_CUDA;
+    return launch_merge_state(o_a, lse_a, o_b, lse_b, rows, head_dim, o_out, lse_out, n_sm,
+                              reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? CPA_OK
+               : CPA_ERR_LAUNCH;
+}
+
+size_t cpa_prefill_hit_workspace_size(int B, int N, int H_hit, int H_q, int H_kv, int head_dim,
+                                      int page_size) {
+    if (B < 1 || N < 1 || H_hit < 0 || H_hit > N || H_q < 1 || H_kv < 1 || H_q % H_kv ||
+        head_dim != 128 || !page_size_ok(page_size))
+        return 0;
+    const int G = H_q / H_kv;
+    if (!pow2(G) || G > 128) return 0;
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return 0;
+    const int TS = 128 / G;
+    const long long QT = ((long long)(N - H_hit) + TS - 1) / TS;
+    return ws_layout((long long)B * H_kv * (QT > 0 ? QT : 1), n_sm).total;
+}
+
+cpa_status cpa_prefill_hit(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* page_table, int pt_stride, int B, int N, int H_hit,
+                           int H_q, int H_kv, int head_dim, int page_size, int num_pages,
+                           float sm_scale, int part, void* o, float* lse, void* workspace,
+                           size_t workspace_bytes, cpa_stream_t stream) {
+    if (!q || !k_pages || !v_pages || !page_table || !o || !lse) return CPA_ERR_INVALID_ARG;
+    if (B < 1 || N < 1 || H_hit < 0 || H_hit > N || H_q < 1 || H_kv < 1 || H_q % H_kv ||
+        num_pages < 1 || !std::isfinite(sm_scale))
+        return CPA_ERR_INVALID_ARG;
+    if (part != CPA_PREFILL_FULL && part != CPA_PREFILL_RECT && part != CPA_PREFILL_TRI)
+        return CPA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o))
+        return CPA_ERR_INVALID_ARG;
+    if (head_dim != 128 || !page_size_ok(page_size)) return CPA_ERR_UNSUPPORTED;
+    const int G = H_q / H_kv;
+    if (!pow2(G) || G > 128) return CPA_ERR_UNSUPPORTED;
+    if (pt_stride < (N + page_size - 1) / page_size) return CPA_ERR_INVALID_ARG;
+    if ((long long)num_pages * page_size > (1ll << 31)) return CPA_ERR_UNSUPPORTED;
+    const int M = N - H_hit;
+    if (M == 0) return CPA_OK;
+    const int TS = 128 / G;
+    Geometry geo;
+    if (!plan_geometry(G, TS, false, true, geo)) return CPA_ERR_UNSUPPORTED;
+    AttnParams p;
+    fill_common(p, q, k_pages, v_pages, page_table, pt_stride, nullptr, 0, nullptr, B, 1, 1, H_q,
+                H_kv, page_size, num_pages, 0, sm_scale);
+    p.mode = part == CPA_PREFILL_FULL ? MODE_PREFILL
+             : part == CPA_PREFILL_RECT ? MODE_PREFILL_RECT
+                                        : MODE_PREFILL_TRI;
+    p.N = N;
+    p.H_hit = H_hit;
+    p.M = M;
+    p.QT = (M + TS - 1) / TS;
+    p.o = o;
+    p.lse = lse;
+    if (!make_map(&p.qmap, q, H_q, (uint64_t)B * M, G, geo.TSB)) return CPA_ERR_CUDA;
+    if (!kv_maps(p, k_pages, v_pages, H_kv, num_pages, page_size)) return CPA_ERR_CUDA;
+    const long long n_units = (long long)B * H_kv * p.QT;
+    return run_attn(p, geo, n_units, workspace, workspace_bytes,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+cpa_status cpa_get_device_status(const void* workspace, uint32_t* status_out,
+                                  cpa_stream_t stream) {
+    if (!workspace || !status_out) return CPA_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return CPA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return CPA_ERR_CUDA;
+    *status_out = v;
+    if (v & CPA_DEV_TIMEOUT) return CPA_ERR_TIMEOUT;
+    if (v & CPA_DEV_BAD_PAGE) return CPA_ERR_BAD_PAGE;
+    if (v & CPA_DEV_BAD_LENGTH) return CPA_ERR_BAD_LENGTH;
+    return CPA_OK;
+}
+
+cpa_status cpa_debug_wait_timeout(void* workspace, size_t workspace_bytes, int limit_us,
+                                  cpa_stream_t stream) {
+    if (!workspace || workspace_bytes < kStatusBytes) return CPA_ERR_WORKSPACE;
+    if (limit_us < 1 || limit_us > 1000000) return CPA_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(workspace, 0, kStatusBytes, s) != cudaSuccess) return CPA_ERR_CUDA;
+    return launch_wait_timeout(static_cast<uint32_t*>(workspace),
+                               (unsigned long long)limit_us * 1000ull, s) == cudaSuccess
+               ? CPA_OK
+               : CPA_ERR_LAUNCH;
+}
+
+int cpa_plan_partition(int64_t total, int n_ctas, int cta, int64_t tile, int64_t* begin,
+                       int64_t* end) {
+    if (total < 1 || n_ctas < 1 || n_ctas > total || cta < 0 || cta >= n_ctas || tile < 0 ||
+        tile >= total)
+        return -1;
+    if (begin) *begin = split_begin(total, n_ctas, cta);
+    if (end) *end = split_begin(total, n_ctas, cta + 1);
+    return split_owner(total, n_ctas, tile);
+}
+
+}  // extern "C"

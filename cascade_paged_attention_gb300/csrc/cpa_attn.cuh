@@ -1,0 +1,984 @@
+// cpa_attn.cuh -- the paged attention kernel behind cascade verify (Pass A
+// with fused Pass B + merge), Pass A alone, naive expand and prefix-hit
+// prefill, for sm_103a.
+//
+// One persistent CTA per SM.  The key tiles of all work units are laid end to
+// end and cut into one contiguous, equal-length range per CTA, so every SM
+// streams the same number of KV bytes whatever the mix of sequence lengths.
+// A unit whose tiles straddle two CTAs is finished by whichever CTA arrives
+// last: each piece writes (o, lse) as a partial and the last one merges them
+// in CTA order with the log-sum-exp identity, so results do not depend on
+// arrival order.
+//
+// Work unit:   cascade / Pass A  one request b and one KV head: its
+//                                topk*S draft tokens x G query heads share
+//                                one read of the prefix (M = topk*S*G rows);
+//              naive expand      one branch (b, k) and one KV head: S*G rows,
+//                                the same prefix read again for every k;
+//              prefill           one KV head and 128/G suffix tokens.
+//
+// Warp roles (warp index w):
+//   w = 0      producer: walks the block table (page ids prefetched 32 boxes
+//              ahead by the whole warp) and issues TMA loads of 128-B
+//              swizzled K/V boxes into a multi-stage ring, and of Q per unit;
+//   w = 1      MMA issuer: S = Q K^T (M=128, N=64, K=128) into TMEM, then
+//              O += P V (M=128, N=128, K=64) into TMEM;
+//   w = 4..    softmax, one warpgroup per 128-row M tile: reads its S row
+//              from TMEM, masks, exponentiates (base 2), writes bf16 P into
+//              swizzled shared memory, and rescales O in TMEM only when the
+//              running max grew by more than 2^8;
+//   last 4     epilogue: O / l, split-piece merge, then (verify) the row's
+//              own-branch draft attention and the final merge, bf16 store.
+// O is double-buffered in TMEM for one M tile, so the epilogue of one unit
+// overlaps the next unit's main loop.
+#pragma once
+#include <cstdint>
+
+#include "cpa_device.cuh"
+#include "cpa_types.h"
+
+namespace cpa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+struct AttnParams {
+    CUtensorMap qmap;
+    CUtensorMap kmap;
+    CUtensorMap vmap;
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k_pages;
+    const __nv_bfloat16* v_pages;
+    const int32_t* ptab;  // prefix table (verify) / sequence table (prefill)
+    const int32_t* dtab;  // draft table (verify)
+    const int32_t* lens;  // prefix lengths (verify)
+    void* o;
+    float* lse;
+    uint32_t* status;
+    uint32_t* counters;
+    float* part_o;    // [2*n_ctas][kMaxUnitRows][128]
+    float* part_lse;  // [2*n_ctas][kMaxUnitRows], log2 units
+    int mode;
+    int B, topk, S, H_q, H_kv, G, P, num_pages;
+    int ptab_stride, dtab_stride, max_len;
+    int N, H_hit, M, QT;  // prefill
+    int upg;              // verify: units per request
+    int TS;               // query tokens per unit
+    int TSB;              // query tokens per M tile
+    int Rq;               // rows of one Q M-tile buffer (multiple of 8)
+    int boxr;             // rows of one K/V TMA box
+    int n_stages, n_qbufs;
+    int draft_keys;       // draft keys staged per unit (cascade topk*S, naive S)
+    float scale_log2;     // sm_scale * log2(e)
+    uint32_t off_q, off_kv, off_p, off_draft;
+};
+
+// ------------------------------------------------------------------ units
+struct Unit {
+    int b, h;
+    int t0, ntok;     // query tokens [t0, t0 + ntok)
+    int p0;           // prefill: suffix position of token t0
+    int branch0;      // verify: first branch of the unit
+    int lo, hi;       // keys [lo, hi) visible (prefill full/tri: hi of the last row)
+    int valid_end;    // keys at or past this are not in the sequence
+    int tile_base;    // first key tile
+    int n_tiles;
+    const int32_t* trow;
+};
+
+__device__ __forceinline__ bool is_verify(int mode) { return mode <= MODE_PASS_A; }
+
+__device__ __forceinline__ int prefix_len(const AttnParams& p, int b) {
+    int L = __ldg(p.lens + b);
+    return L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
+}
+
+__device__ __forceinline__ void prefill_keys(const AttnParams& p, int p0, int ntok, int& lo,
+                                             int& hi) {
+    if (p.mode == MODE_PREFILL_RECT) {
+        lo = 0;
+        hi = p.H_hit;
+    } else if (p.mode == MODE_PREFILL_TRI) {
+        lo = p.H_hit;
+        hi = p.H_hit + p0 + ntok;
+    } else {
+        lo = 0;
+        hi = p.H_hit + p0 + ntok;
+    }
+}
+
+__device__ __forceinline__ int tiles_for(int lo, int hi) {
+    int t = (hi + kBN - 1) / kBN - lo / kBN;
+    return t < 1 ? 1 : t;
+}
+
+__device__ __forceinline__ int prefill_qt_tiles(const AttnParams& p, int qt) {
+    int p0 = qt * p.TS;
+    int ntok = min(p.TS, p.M - p0);
+    int lo, hi;
+    prefill_keys(p, p0, ntok, lo, hi);
+    return tiles_for(lo, hi);
+}
+
+__device__ __forceinline__ Unit get_unit(const AttnParams& p, int u) {
+    Unit x;
+    if (is_verify(p.mode)) {
+        const int b = u / p.upg, rem = u % p.upg;
+        const int L = prefix_len(p, b);
+        x.b = b;
+        x.lo = 0;
+        x.hi = L;
+        x.valid_end = L;
+        x.tile_base = 0;
+        x.n_tiles = L > 0 ? (L + kBN - 1) / kBN : 1;
+        x.p0 = 0;
+        x.trow = p.ptab + (size_t)b * p.ptab_stride;
+        if (p.mode == MODE_NAIVE) {
+            const int k = rem / p.H_kv;
+            x.h = rem % p.H_kv;
+            x.branch0 = k;
+            x.t0 = (b * p.topk + k) * p.S;
+            x.ntok = p.S;
+        } else {
+            x.h = rem;
+            x.branch0 = 0;
+            x.t0 = b * p.TS;
+            x.ntok = p.TS;
+        }
+    } else {
+        const int grp = u / p.QT, qt = u % p.QT;
+        x.b = grp / p.H_kv;
+        x.h = grp % p.H_kv;
+        x.p0 = qt * p.TS;
+        x.ntok = min(p.TS, p.M - x.p0);
+        x.t0 = x.b * p.M + x.p0;
+        x.valid_end = p.N;
+        x.branch0 = 0;
+        prefill_keys(p, x.p0, x.ntok, x.lo, x.hi);
+        x.tile_base = x.lo / kBN;
+        x.n_tiles = tiles_for(x.lo, x.hi);
+        x.trow = p.ptab + (size_t)x.b * p.ptab_stride;
+    }
+    return x;
+}
+
+// ------------------------------------------------------------------ shared control block
+struct Ctrl {
+    uint64_t kv_full[4], kv_empty[4];
+    uint64_t q_full[2], q_empty[2];
+    uint64_t s_full[2], p_full[2], p_empty[2];
+    uint64_t o_full[2], o_empty[2], stats_full[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+    int64_t total;   // tiles of the whole problem
+    int64_t begin;   // this CTA's first tile
+    int64_t count;   // this CTA's tiles
+    int64_t ustart;  // global tile index where the first unit starts
+    int n_ctas;      // CTAs that have work
+    int u0, j0;      // first unit and its first tile
+    int flag;
+    int found;
+    long long scan[32];
+};
+static_assert(sizeof(Ctrl) <= 1024, "control block");
+
+constexpr uint32_t kOffStats = 1024;  // float2 [2][256] of (max, sum) per row: 4 KB
+constexpr uint32_t kOffData = 5120;   // first 1024-aligned byte after the stats
+constexpr uint32_t kStageBytes = 4u * kBN * 128u;
+constexpr uint32_t kPBytes = 128u * 128u;
+
+template <int NUM_MT>
+struct Cfg {
+    static constexpr int kPBufs = NUM_MT == 1 ? 2 : 1;
+    static constexpr int kOBufs = NUM_MT == 1 ? 2 : 1;
+    static constexpr int kSmWarp0 = 4;
+    static constexpr int kEpiWarp0 = 4 + 4 * NUM_MT;
+    static constexpr int kThreads = 32 * (kEpiWarp0 + 4);
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t s_col(int mt, int sb) { return (uint32_t)(mt * 2 + sb) * kBN; }
+    static constexpr uint32_t o_col(int mt, int ob) {
+        return (uint32_t)(NUM_MT * 2 * kBN) + (uint32_t)(mt * kOBufs + ob) * 128u;
+    }
+};
+
+// Inclusive block-wide prefix sum of one int64 per thread; returns the
+// exclusive prefix and the block total.
+__device__ __forceinline__ long long block_scan(long long v, long long* ws, long long& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) ws[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = lane < nw ? ws[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            long long y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        ws[lane] = w;
+    }
+    __syncthreads();
+    const long long base = warp > 0 ? ws[warp - 1] : 0;
+    total = ws[nw - 1];
+    __syncthreads();
+    return base + x - v;
+}
+
+// Every thread of the CTA: find the problem's total tile count and where this
+// CTA's range begins.
+__device__ __forceinline__ void schedule(const AttnParams& p, Ctrl* c) {
+    long long total = 0;
+    const int nthr = blockDim.x;
+    if (is_verify(p.mode)) {
+        // group = request; every unit of a request has the same tile count
+        for (int b0 = 0; b0 < p.B; b0 += nthr) {
+            const int b = b0 + threadIdx.x;
+            long long v = 0;
+            if (b < p.B) {
+                const int L = __ldg(p.lens + b);
+                if (L < 0 || L > p.max_len) atomicOr(p.status, CPA_DEV_BAD_LENGTH);
+                const int Lc = prefix_len(p, b);
+                v = (long long)p.upg * (Lc > 0 ? (Lc + kBN - 1) / kBN : 1);
+            }
+            long long tot;
+            block_scan(v, c->scan, tot);
+            total += tot;
+        }
+    } else {
+        long long gt = 0;
+        for (int qt = 0; qt < p.QT; ++qt) gt += prefill_qt_tiles(p, qt);
+        total = gt * p.B * p.H_kv;
+    }
+    const int n_ctas = (int)(total < (long long)gridDim.x ? total : (long long)gridDim.x);
+    const int cta = blockIdx.x;
+    if (threadIdx.x == 0) {
+        c->total = total;
+        c->n_ctas = n_ctas;
+        c->found = 0;
+        if (cta < n_ctas) {
+            c->begin = split_begin(total, n_ctas, cta);
+            c->count = split_begin(total, n_ctas, cta + 1) - c->begin;
+        } else {
+            c->begin = 0;
+            c->count = 0;
+        }
+    }
+    __syncthreads();
+    if (c->count == 0) return;
+    const long long t0 = c->begin;
+    if (is_verify(p.mode)) {
+        long long run = 0;
+        for (int b0 = 0; b0 < p.B; b0 += nthr) {
+            const int b = b0 + threadIdx.x;
+            long long v = 0;
+            int tpu = 1;
+            if (b < p.B) {
+                const int Lc = prefix_len(p, b);
+                tpu = Lc > 0 ? (Lc + kBN - 1) / kBN : 1;
+                v = (long long)p.upg * tpu;
+            }
+            long long tot;
+            const long long ex = block_scan(v, c->scan, tot);
+            if (b < p.B && run + ex <= t0 && t0 < run + ex + v) {
+                const long long off = t0 - (run + ex);
+                c->u0 = b * p.upg + (int)(off / tpu);
+                c->j0 = (int)(off % tpu);
+                c->ustart = run + ex + (off / tpu) * tpu;
+                c->found = 1;
+            }
+            run += tot;
+            __syncthreads();
+            if (c->found) break;
+        }
+    } else if (threadIdx.x == 0) {
+        long long gt = 0;
+        for (int qt = 0; qt < p.QT; ++qt) gt += prefill_qt_tiles(p, qt);
+        const long long grp = t0 / gt;
+        long long acc = grp * gt;
+        for (int qt = 0; qt < p.QT; ++qt) {
+            const int n = prefill_qt_tiles(p, qt);
+            if (t0 < acc + n) {
+                c->u0 = (int)(grp * p.QT + qt);
+                c->j0 = (int)(t0 - acc);
+                c->ustart = acc;
+                break;
+            }
+            acc += n;
+        }
+        c->found = 1;
+    }
+    __syncthreads();
+}
+
+// Walks this CTA's tiles unit by unit; every role runs its own copy.
+struct Walker {
+    int u, j;
+    long long ustart;
+    long long left;
+    int seg;
+    __device__ __forceinline__ void init(const Ctrl* c) {
+        u = c->u0;
+        j = c->j0;
+        ustart = c->ustart;
+        left = c->count;
+        seg = 0;
+    }
+    // Tiles [jb, je) of unit x that belong to this CTA.
+    __device__ __forceinline__ void piece(const Unit& x, int& jb, int& je) const {
+        jb = j;
+        const long long rest = (long long)x.n_tiles - j;
+        je = (int)(j + (left < rest ? left : rest));
+    }
+    __device__ __forceinline__ void next(const Unit& x, int jb, int je) {
+        left -= (je - jb);
+        ustart += x.n_tiles;
+        ++u;
+        j = 0;
+        ++seg;
+    }
+};
+
+// ------------------------------------------------------------------ epilogue helpers
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+template <int NUM_MT>
+__global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
+    paged_attn_kernel(const __grid_constant__ AttnParams p) {
+    using C = Cfg<NUM_MT>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem);
+    float2* stats = reinterpret_cast<float2*>(smem + kOffStats);
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile uint32_t* abort_flag = &ctrl->abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&ctrl->kv_full[i], 1);
+            mbar_init(&ctrl->kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctrl->q_full[i], 1);
+            mbar_init(&ctrl->q_empty[i], 1);
+            mbar_init(&ctrl->s_full[i], 1);
+            mbar_init(&ctrl->p_full[i], 128 * NUM_MT);
+            mbar_init(&ctrl->p_empty[i], 1);
+            mbar_init(&ctrl->o_full[i], 1);
+            mbar_init(&ctrl->o_empty[i], 128);
+            mbar_init(&ctrl->stats_full[i], 128 * NUM_MT);
+        }
+        mbar_init(&ctrl->mma_done, 1);
+        ctrl->abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&p.qmap);
+        prefetch_tmap(&p.kmap);
+        prefetch_tmap(&p.vmap);
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctrl->tmem_base, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    schedule(p, ctrl);
+    const uint32_t tmem = ctrl->tmem_base;
+    const int n_ctas = ctrl->n_ctas;
+    const long long total = ctrl->total;
+    const int G = p.G;
+
+    if (ctrl->count > 0) {
+        if (warp == 0) {
+            // ============================== producer
+            const uint64_t pol_kv = l2_policy_evict_first();
+            const uint64_t pol_q = l2_policy_evict_last();
+            const int NB = kBN / p.boxr;
+            const uint32_t q_tx = (uint32_t)(NUM_MT * 2 * G * p.TSB * 128);
+            const uint32_t qmt_bytes = (uint32_t)(2 * p.Rq * 128);
+            Walker w;
+            w.init(ctrl);
+            long long g = 0;
+            bool ok = true;
+            while (w.left > 0 && ok) {
+                const Unit x = get_unit(p, w.u);
+                int jb, je;
+                w.piece(x, jb, je);
+                const int qb = w.seg % p.n_qbufs;
+                if (w.seg >= p.n_qbufs)
+                    ok = mbar_wait_warp(&ctrl->q_empty[qb], ((w.seg / p.n_qbufs) - 1) & 1, abort_flag,
+                                   p.status);
+                if (!ok) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&ctrl->q_full[qb], q_tx);
+                    for (int mt = 0; mt < NUM_MT; ++mt) {
+                        uint8_t* dst = smem + p.off_q + (qb * NUM_MT + mt) * qmt_bytes;
+                        const int tok = x.t0 + mt * p.TSB;
+                        tma_load_3d(dst, &p.qmap, 0, x.h * G, tok, &ctrl->q_full[qb], pol_q);
+                        tma_load_3d(dst + p.Rq * 128, &p.qmap, 64, x.h * G, tok,
+                                    &ctrl->q_full[qb], pol_q);
+                    }
+                }
+                // block-table window: lane l holds the page of box (wbase + l)
+                const int key_base = x.tile_base * kBN;
+                auto load_page = [&](int box) -> int {
+                    const int pos = key_base + box * p.boxr;
+                    return pos < x.valid_end ? __ldg(x.trow + pos / p.P) : -1;
+                };
+                int wbase = jb * NB;
+                int cur = load_page(wbase + lane);
+                int nxt = load_page(wbase + 32 + lane);
+                for (int jj = jb; jj < je; ++jj, ++g) {
+                    const int st = (int)(g % p.n_stages);
+                    if (g >= p.n_stages) {
+                        ok = mbar_wait_warp(&ctrl->kv_empty[st], (uint32_t)(((g / p.n_stages) - 1) & 1),
+                                       abort_flag, p.status);
+                        if (!ok) break;
+                    }
+                    const int box0 = jj * NB;
+                    if (box0 >= wbase + 32) {
+                        cur = nxt;
+                        wbase += 32;
+                        nxt = load_page(wbase + 32 + lane);
+                    }
+                    const int my_box = box0 + (lane & (NB - 1));
+                    int pg = __shfl_sync(0xffffffffu, cur, (my_box - wbase) & 31);
+                    const int pos = key_base + my_box * p.boxr;
+                    bool use = lane < NB && pos < x.valid_end;
+                    if (use && (pg < 0 || pg >= p.num_pages)) {
+                        atomicOr(p.status, CPA_DEV_BAD_PAGE);
+                        use = false;
+                    }
+                    const uint32_t mask = __ballot_sync(0xffffffffu, use);
+                    if (lane == 0) {
+                        const uint32_t bytes = (uint32_t)__popc(mask) * 4u * p.boxr * 128u;
+                        mbar_arrive_expect_tx(&ctrl->kv_full[st], bytes);
+                    }
+                    uint8_t* sk = smem + p.off_kv + st * kStageBytes;
+                    for (int i = 0; i < NB; ++i) {
+                        const int pgi = __shfl_sync(0xffffffffu, pg, i);
+                        if (lane == 0 && (mask >> i & 1u)) {
+                            const int posi = key_base + (box0 + i) * p.boxr;
+                            const int row = pgi * p.P + (posi % p.P);
+                            uint8_t* dk = sk + i * p.boxr * 128;
+                            tma_load_3d(dk, &p.kmap, 0, x.h, row, &ctrl->kv_full[st], pol_kv);
+                            tma_load_3d(dk + kBN * 128, &p.kmap, 64, x.h, row, &ctrl->kv_full[st],
+                                        pol_kv);
+                            tma_load_3d(dk + 2 * kBN * 128, &p.vmap, 0, x.h, row,
+                                        &ctrl->kv_full[st], pol_kv);
+                            tma_load_3d(dk + 3 * kBN * 128, &p.vmap, 64, x.h, row,
+                                        &ctrl->kv_full[st], pol_kv);
+                        }
+                    }
+                }
+                w.next(x, jb, je);
+            }
+            // make sure no TMA write is still in flight when the CTA leaves
+            const long long filled = g;
+            for (int st = 0; st < p.n_stages; ++st) {
+                if (st < filled) {
+                    const long long last = st + ((filled - 1 - st) / p.n_stages) * p.n_stages;
+                    mbar_wait(&ctrl->kv_full[st], (uint32_t)((last / p.n_stages) & 1), abort_flag,
+                              p.status);
+                }
+            }
+        } else if (warp == 1) {
+            // ============================== MMA issuer
+            if (lane == 0) {
+                const uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
+                const uint32_t idesc_o = idesc_bf16_f32(128, 128, true);
+                const uint32_t qmt_bytes = (uint32_t)(2 * p.Rq * 128);
+                Walker w;
+                w.init(ctrl);
+                long long g = 0;
+                bool ok = true;
+                bool have_prev = false;
+                long long pg_ = 0;
+                int pst = 0, pseg = 0, pob = 0;
+                bool pfirst = false, plast = false;
+                auto issue_pv = [&]() -> bool {
+                    if (!mbar_wait(&ctrl->p_full[pg_ & 1], (uint32_t)((pg_ >> 1) & 1), abort_flag,
+                                   p.status))
+                        return false;
+                    if (pfirst && pseg >= C::kOBufs) {
+                        if (!mbar_wait(&ctrl->o_empty[pob], ((pseg / C::kOBufs) - 1) & 1,
+                                       abort_flag, p.status))
+                            return false;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t vb = sbase + p.off_kv + pst * kStageBytes + 2 * kBN * 128;
+                    for (int mt = 0; mt < NUM_MT; ++mt) {
+                        const uint32_t pa =
+                            sbase + p.off_p + (mt * C::kPBufs + (int)(pg_ % C::kPBufs)) * kPBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk) {
+                            const uint64_t a = sdesc_sw128(pa + kk * 32, 16, 1024);
+                            const uint64_t b = sdesc_sw128(vb + kk * 16 * 128, kBN * 128, 1024);
+                            umma_bf16_ss(tmem + C::o_col(mt, pob), a, b, idesc_o,
+                                         (pfirst && kk == 0) ? 0u : 1u);
+                        }
+                    }
+                    umma_commit(&ctrl->p_empty[pg_ & 1]);
+                    umma_commit(&ctrl->kv_empty[pst]);
+                    if (plast) umma_commit(&ctrl->o_full[pob]);
+                    return true;
+                };
+                while (w.left > 0 && ok) {
+                    const Unit x = get_unit(p, w.u);
+                    int jb, je;
+                    w.piece(x, jb, je);
+                    const int qb = w.seg % p.n_qbufs;
+                    const int ob = w.seg % C::kOBufs;
+                    ok = mbar_wait(&ctrl->q_full[qb], (w.seg / p.n_qbufs) & 1, abort_flag,
+                                   p.status);
+                    if (!ok) break;
+                    for (int jj = jb; jj < je; ++jj, ++g) {
+                        const int st = (int)(g % p.n_stages);
+                        ok = mbar_wait(&ctrl->kv_full[st], (uint32_t)((g / p.n_stages) & 1),
+                                       abort_flag, p.status);
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        const int sb = (int)(g & 1);
+                        const uint32_t kb = sbase + p.off_kv + st * kStageBytes;
+                        for (int mt = 0; mt < NUM_MT; ++mt) {
+                            const uint32_t qa = sbase + p.off_q + (qb * NUM_MT + mt) * qmt_bytes;
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t a = sdesc_sw128(
+                                    qa + (kk >> 2) * p.Rq * 128 + (kk & 3) * 32, 16, 1024);
+                                const uint64_t b = sdesc_sw128(
+                                    kb + (kk >> 2) * kBN * 128 + (kk & 3) * 32, 16, 1024);
+                                umma_bf16_ss(tmem + C::s_col(mt, sb), a, b, idesc_s,
+                                             kk > 0 ? 1u : 0u);
+                            }
+                        }
+                        umma_commit(&ctrl->s_full[sb]);
+                        if (jj == je - 1) umma_commit(&ctrl->q_empty[qb]);
+                        if (have_prev) {
+                            ok = issue_pv();
+                            if (!ok) break;
+                        }
+                        pg_ = g;
+                        pst = st;
+                        pseg = w.seg;
+                        pob = ob;
+                        pfirst = (jj == jb);
+                        plast = (jj == je - 1);
+                        have_prev = true;
+                    }
+                    w.next(x, jb, je);
+                }
+                if (ok && have_prev) issue_pv();
+                umma_commit(&ctrl->mma_done);
+                mbar_wait(&ctrl->mma_done, 0, abort_flag, p.status);
+            }
+            __syncwarp();
+        } else if (warp >= C::kSmWarp0 && warp < C::kEpiWarp0) {
+            // ============================== softmax
+            const int mt = (warp - C::kSmWarp0) >> 2;
+            const int quarter = warp & 3;
+            const int r = quarter * 32 + lane;
+            const int R = mt * 128 + r;
+            const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+            Walker w;
+            w.init(ctrl);
+            long long g = 0;
+            bool ok = true;
+            while (w.left > 0 && ok) {
+                const Unit x = get_unit(p, w.u);
+                int jb, je;
+                w.piece(x, jb, je);
+                const int ob = w.seg % C::kOBufs;
+                const int it = R / G;
+                int lo = x.lo, hi;
+                if (is_verify(p.mode) || p.mode == MODE_PREFILL_RECT) hi = x.hi;
+                else hi = p.H_hit + x.p0 + it + 1;
+                if (it >= x.ntok) hi = lo;  // rows past the unit's tokens see nothing
+                float m_used = neg_inf(), l = 0.f;
+                const uint32_t o_addr = tmem + lane_addr + C::o_col(mt, ob);
+                for (int jj = jb; jj < je; ++jj, ++g) {
+                    ok = mbar_wait_warp(&ctrl->s_full[g & 1], (uint32_t)((g >> 1) & 1), abort_flag,
+                                   p.status);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    uint32_t sr[64];
+                    tmem_ld_x64(tmem + lane_addr + C::s_col(mt, (int)(g & 1)), sr);
+                    const int key0 = (x.tile_base + jj) * kBN;
+                    const bool whole = key0 >= lo && key0 + kBN <= hi;
+                    float tmax = neg_inf();
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const int key = key0 + c;
+                        const float s = __uint_as_float(sr[c]) * p.scale_log2;
+                        const float v = (whole || (key >= lo && key < hi)) ? s : neg_inf();
+                        sr[c] = __float_as_uint(v);
+                        tmax = fmaxf(tmax, v);
+                    }
+                    const bool need = (l > 0.f) && (tmax > m_used + kRescaleLog2);
+                    if (__any_sync(0xffffffffu, need)) {
+                        // O holds PV of tiles up to g-1 of this unit: wait for it, then rescale
+                        ok = mbar_wait_warp(&ctrl->p_empty[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1),
+                                       abort_flag, p.status);
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        const float f = need ? ex2(m_used - tmax) : 1.f;
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            uint32_t ov[32];
+                            tmem_ld_x32(o_addr + c4 * 32, ov);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+                            tmem_st_x32(o_addr + c4 * 32, ov);
+                        }
+                        if (need) {
+                            l *= f;
+                            m_used = tmax;
+                        }
+                    }
+                    if (m_used == neg_inf()) m_used = tmax;
+                    const float mref = (m_used == neg_inf()) ? 0.f : m_used;
+                    float sum = 0.f;
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const float a = ex2(__uint_as_float(sr[2 * c]) - mref);
+                        const float b = ex2(__uint_as_float(sr[2 * c + 1]) - mref);
+                        sum += a + b;
+                        pk[c] = pack_bf16x2(a, b);
+                    }
+                    l += sum;
+                    // the P buffer this tile writes must no longer be read by an earlier PV
+                    if (C::kPBufs == 2) {
+                        if (g >= 2)
+                            ok = mbar_wait_warp(&ctrl->p_empty[g & 1], (uint32_t)(((g - 2) >> 1) & 1),
+                                           abort_flag, p.status);
+                    } else if (g >= 1) {
+                        ok = mbar_wait_warp(&ctrl->p_empty[(g - 1) & 1],
+                                       (uint32_t)(((g - 1) >> 1) & 1), abort_flag, p.status);
+                    }
+                    if (!ok) break;
+                    uint8_t* prow = smem + p.off_p + (mt * C::kPBufs + (int)(g % C::kPBufs)) * kPBytes +
+                                    r * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    if (mt == 0 && key0 + kBN > x.valid_end) {
+                        // V rows past the sequence end hold whatever the page had (or stale
+                        // data): zero them so that P = 0 there contributes exactly nothing.
+                        const int first = max(0, x.valid_end - key0);
+                        const int st = (int)(g % p.n_stages);
+                        uint8_t* vb = smem + p.off_kv + st * kStageBytes + 2 * kBN * 128;
+                        const int n16 = (kBN - first) * 8;  // 16-B chunks per half
+                        for (int i = r; i < 2 * n16; i += 128) {
+                            const int half = i / n16, rem = i % n16;
+                            *reinterpret_cast<uint4*>(vb + half * kBN * 128 + first * 128 + rem * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before_sync();
+                    mbar_arrive(&ctrl->p_full[g & 1]);
+                }
+                if (!ok) break;
+                if (w.seg >= C::kOBufs) {
+                    ok = mbar_wait_warp(&ctrl->o_empty[ob], ((w.seg / C::kOBufs) - 1) & 1, abort_flag,
+                                   p.status);
+                    if (!ok) break;
+                }
+                stats[ob * 256 + R] = make_float2(m_used, l);
+                mbar_arrive(&ctrl->stats_full[ob]);
+                w.next(x, jb, je);
+            }
+        } else if (warp >= C::kEpiWarp0) {
+            // ============================== epilogue
+            const int quarter = warp & 3;
+            const int r = quarter * 32 + lane;
+            const int et = r;  // 0..127 within the epilogue warpgroup
+            const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+            const bool verify_out = p.mode == MODE_CASCADE || p.mode == MODE_NAIVE;
+            const bool fp32_out = p.mode == MODE_PASS_A || p.mode == MODE_PREFILL_RECT ||
+                                  p.mode == MODE_PREFILL_TRI;
+            uint8_t* dk_s = smem + p.off_draft;
+            uint8_t* dv_s = dk_s + kMaxDraftKeys * 256;
+            Walker w;
+            w.init(ctrl);
+            bool ok = true;
+            while (w.left > 0 && ok) {
+                const Unit x = get_unit(p, w.u);
+                int jb, je;
+                w.piece(x, jb, je);
+                const bool split = jb > 0 || je < x.n_tiles;
+                const int ob = w.seg % C::kOBufs;
+                const uint32_t ph = (uint32_t)((w.seg / C::kOBufs) & 1);
+                ok = mbar_wait(&ctrl->o_full[ob], ph, abort_flag, p.status) &&
+                     mbar_wait(&ctrl->stats_full[ob], ph, abort_flag, p.status);
+                ok = bar_and(1, 128, ok);  // one decision for the whole epilogue warpgroup
+                if (!ok) break;
+                tc_fence_after_sync();
+
+                // stage this unit's draft K/V rows (verify) in shared memory
+                auto load_draft = [&]() {
+                    const int nk = p.draft_keys;
+                    for (int i = et; i < nk * 32; i += 128) {
+                        const int kx = i >> 5, part = i & 31;  // 16 chunks of K then 16 of V
+                        const int br = x.branch0 + kx / p.S, j = kx % p.S;
+                        const int pg = __ldg(p.dtab + (size_t)(x.b * p.topk + br) * p.dtab_stride +
+                                             j / p.P);
+                        uint4 v = make_uint4(0, 0, 0, 0);
+                        if (pg >= 0 && pg < p.num_pages) {
+                            const size_t off =
+                                (((size_t)pg * p.P + (j % p.P)) * p.H_kv + x.h) * 128 +
+                                (part & 15) * 8;
+                            const __nv_bfloat16* src = (part < 16 ? p.k_pages : p.v_pages) + off;
+                            v = __ldg(reinterpret_cast<const uint4*>(src));
+                        } else if (part == 0) {
+                            atomicOr(p.status, CPA_DEV_BAD_PAGE);
+                        }
+                        uint8_t* dst = (part < 16 ? dk_s : dv_s) + kx * 256 + (part & 15) * 16;
+                        *reinterpret_cast<uint4*>(dst) = v;
+                    }
+                };
+
+                // write one row's result; oa(c, f[8]) supplies o_A / sum for chunk c
+                auto finish_row = [&](int R, float lse2a, auto&& oa) {
+                    const int it = R / G, gq = R % G;
+                    const bool valid = it < x.ntok;
+                    const size_t orow = (size_t)(x.t0 + (valid ? it : 0)) * p.H_q + x.h * G + gq;
+                    if (!verify_out) {
+#pragma unroll 1
+                        for (int c = 0; c < 16; ++c) {
+                            float f[8];
+                            oa(c, f);
+                            if (valid) {
+                                if (fp32_out) {
+                                    float4* dst = reinterpret_cast<float4*>(
+                                        static_cast<float*>(p.o) + orow * 128 + c * 8);
+                                    dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+                                    dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+                                } else {
+                                    *reinterpret_cast<uint4*>(
+                                        static_cast<__nv_bfloat16*>(p.o) + orow * 128 + c * 8) =
+                                        make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                                   pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                                }
+                            }
+                        }
+                        if (valid) p.lse[orow] = lse2a == neg_inf() ? neg_inf() : lse2a * kLn2;
+                        return;
+                    }
+                    // own-branch drafts 0..s (Pass B) for this row, then the LSE merge
+                    const int sidx = valid ? it % p.S : 0;
+                    const int kb = (valid && p.mode == MODE_CASCADE) ? (it / p.S) * p.S : 0;
+                    const __nv_bfloat16* qrow = p.q + orow * 128;
+                    float sc[kMaxDraft];
+#pragma unroll
+                    for (int j = 0; j < kMaxDraft; ++j) sc[j] = 0.f;
+#pragma unroll 1
+                    for (int c = 0; c < 16; ++c) {
+                        float qf[8];
+                        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(qrow + c * 8)), qf);
+#pragma unroll
+                        for (int j = 0; j < kMaxDraft; ++j) {
+                            if (j <= sidx) {
+                                float kf[8];
+                                bf16x8_to_f32(*reinterpret_cast<const uint4*>(
+                                                  dk_s + (kb + j) * 256 + c * 16),
+                                              kf);
+                                float acc = sc[j];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) acc = fmaf(qf[e], kf[e], acc);
+                                sc[j] = acc;
+                            }
+                        }
+                    }
+                    float mb = neg_inf();
+#pragma unroll
+                    for (int j = 0; j < kMaxDraft; ++j) {
+                        sc[j] *= p.scale_log2;
+                        if (j <= sidx) mb = fmaxf(mb, sc[j]);
+                    }
+                    float lb = 0.f;
+#pragma unroll
+                    for (int j = 0; j < kMaxDraft; ++j) {
+                        sc[j] = (j <= sidx) ? ex2(sc[j] - mb) : 0.f;
+                        lb += sc[j];
+                    }
+                    const float lse2b = mb + lg2(lb);
+                    const float mx = fmaxf(lse2a, lse2b);
+                    const float wa = ex2(lse2a - mx), wb = ex2(lse2b - mx);
+                    const float tot = wa + wb;
+                    const float ca = wa / tot, cb = wb / (tot * lb);
+                    const float lse2 = mx + lg2(tot);
+#pragma unroll 1
+                    for (int c = 0; c < 16; ++c) {
+                        float f[8];
+                        __syncwarp();
+                        oa(c, f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] *= ca;
+#pragma unroll
+                        for (int j = 0; j < kMaxDraft; ++j) {
+                            if (j <= sidx) {
+                                float vf[8];
+                                bf16x8_to_f32(*reinterpret_cast<const uint4*>(
+                                                  dv_s + (kb + j) * 256 + c * 16),
+                                              vf);
+                                const float wj = cb * sc[j];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) f[e] = fmaf(wj, vf[e], f[e]);
+                            }
+                        }
+                        if (valid)
+                            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+                                                      orow * 128 + c * 8) =
+                                make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                           pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                    }
+                    if (valid) p.lse[orow] = lse2 * kLn2;
+                };
+
+                if (!split) {
+                    if (verify_out) {
+                        load_draft();
+                        named_bar_sync(1, 128);
+                    }
+                    for (int mt = 0; mt < NUM_MT; ++mt) {
+                        const int R = mt * 128 + r;
+                        const float2 st = stats[ob * 256 + R];
+                        const float lse2a = st.y > 0.f ? st.x + lg2(st.y) : neg_inf();
+                        const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
+                        const uint32_t oaddr = tmem + lane_addr + C::o_col(mt, ob);
+                        finish_row(R, lse2a, [&](int c, float (&f)[8]) {
+                            uint32_t v[8];
+                            tmem_ld_x8(oaddr + c * 8, v);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[e]) * inv;
+                        });
+                    }
+                    tc_fence_before_sync();
+                    mbar_arrive(&ctrl->o_empty[ob]);
+                    if (verify_out) named_bar_sync(1, 128);  // draft buffer reuse
+                } else {
+                    const int slot = split_slot(total, n_ctas, blockIdx.x, w.ustart);
+                    for (int mt = 0; mt < NUM_MT; ++mt) {
+                        const int R = mt * 128 + r;
+                        const float2 st = stats[ob * 256 + R];
+                        const float lse2a = st.y > 0.f ? st.x + lg2(st.y) : neg_inf();
+                        const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
+                        const uint32_t oaddr = tmem + lane_addr + C::o_col(mt, ob);
+                        const bool valid = R / G < x.ntok;
+                        float* po = p.part_o + ((size_t)slot * kMaxUnitRows + R) * 128;
+#pragma unroll 1
+                        for (int c = 0; c < 16; ++c) {
+                            uint32_t v[8];
+                            tmem_ld_x8(oaddr + c * 8, v);
+                            if (valid) {
+                                float4* d4 = reinterpret_cast<float4*>(po + c * 8);
+                                d4[0] = make_float4(__uint_as_float(v[0]) * inv,
+                                                    __uint_as_float(v[1]) * inv,
+                                                    __uint_as_float(v[2]) * inv,
+                                                    __uint_as_float(v[3]) * inv);
+                                d4[1] = make_float4(__uint_as_float(v[4]) * inv,
+                                                    __uint_as_float(v[5]) * inv,
+                                                    __uint_as_float(v[6]) * inv,
+                                                    __uint_as_float(v[7]) * inv);
+                            }
+                        }
+                        if (valid) p.part_lse[(size_t)slot * kMaxUnitRows + R] = lse2a;
+                    }
+                    tc_fence_before_sync();
+                    mbar_arrive(&ctrl->o_empty[ob]);
+                    __threadfence();
+                    named_bar_sync(1, 128);
+                    if (et == 0) {
+                        const int c_first = split_owner(total, n_ctas, w.ustart);
+                        const int c_last = split_owner(total, n_ctas, w.ustart + x.n_tiles - 1);
+                        const unsigned old = atomicAdd(p.counters + w.u, 1u);
+                        ctrl->flag = (old == (unsigned)(c_last - c_first)) ? 1 : 0;
+                    }
+                    named_bar_sync(1, 128);
+                    const bool last = *reinterpret_cast<volatile int*>(&ctrl->flag) != 0;
+                    if (last) {
+                        __threadfence();
+                        if (verify_out) {
+                            load_draft();
+                            named_bar_sync(1, 128);
+                        }
+                        const int c_first = split_owner(total, n_ctas, w.ustart);
+                        const int c_last = split_owner(total, n_ctas, w.ustart + x.n_tiles - 1);
+                        for (int mt = 0; mt < NUM_MT; ++mt) {
+                            const int R = mt * 128 + r;
+                            const bool valid = R / G < x.ntok;
+                            float mx = neg_inf();
+                            if (valid)
+                                for (int c = c_first; c <= c_last; ++c)
+                                    mx = fmaxf(mx, __ldcg(p.part_lse +
+                                                          (size_t)split_slot(total, n_ctas, c,
+                                                                             w.ustart) *
+                                                              kMaxUnitRows +
+                                                          R));
+                            float den = 0.f;
+                            if (valid && mx != neg_inf())
+                                for (int c = c_first; c <= c_last; ++c)
+                                    den += ex2(__ldcg(p.part_lse +
+                                                      (size_t)split_slot(total, n_ctas, c,
+                                                                         w.ustart) *
+                                                          kMaxUnitRows +
+                                                      R) -
+                                               mx);
+                            const float lse2a = (den > 0.f) ? mx + lg2(den) : neg_inf();
+                            finish_row(R, lse2a, [&](int ch, float (&f)[8]) {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) f[e] = 0.f;
+                                if (!valid || den == 0.f) return;
+                                for (int c = c_first; c <= c_last; ++c) {
+                                    const size_t sl =
+                                        (size_t)split_slot(total, n_ctas, c, w.ustart) *
+                                            kMaxUnitRows +
+                                        R;
+                                    const float wc = ex2(__ldcg(p.part_lse + sl) - lse2a);
+                                    const float4* s4 =
+                                        reinterpret_cast<const float4*>(p.part_o + sl * 128 + ch * 8);
+                                    const float4 a = __ldcg(s4), b = __ldcg(s4 + 1);
+                                    f[0] = fmaf(wc, a.x, f[0]);
+                                    f[1] = fmaf(wc, a.y, f[1]);
+                                    f[2] = fmaf(wc, a.z, f[2]);
+                                    f[3] = fmaf(wc, a.w, f[3]);
+                                    f[4] = fmaf(wc, b.x, f[4]);
+                                    f[5] = fmaf(wc, b.y, f[5]);
+                                    f[6] = fmaf(wc, b.z, f[6]);
+                                    f[7] = fmaf(wc, b.w, f[7]);
+                                }
+                            });
+                        }
+                        if (verify_out) named_bar_sync(1, 128);
+                    }
+                }
+                w.next(x, jb, je);
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+}  // namespace cpa

@@ -1,0 +1,149 @@
+// cpa_small.cu -- the light kernels of the library: merge_state, the
+// stand-alone Pass B draft kernel, and the bounded-wait check.
+#include <cuda_runtime.h>
+
+#include "cpa_device.cuh"
+#include "cpa_small.h"
+
+namespace cpa {
+
+namespace {
+constexpr float kLog2eF = 1.4426950408889634f;
+constexpr float kLn2F = 0.6931471805599453f;
+
+__device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
+}  // namespace
+
+// merge_state ("Cascade attention" page, split property):
+//   lse = log(e^a + e^b), o = e^(a-lse) o_a + e^(b-lse) o_b,
+// evaluated about m = max(a, b).  One thread per 4 consecutive elements of a
+// row; consecutive threads cover consecutive addresses (16-B loads, 8-B stores).
+__global__ void __launch_bounds__(256) merge_state_kernel(const float* __restrict__ o_a,
+                                                          const float* __restrict__ lse_a,
+                                                          const float* __restrict__ o_b,
+                                                          const float* __restrict__ lse_b,
+                                                          long long n_rows, int d4,
+                                                          __nv_bfloat16* __restrict__ o_out,
+                                                          float* __restrict__ lse_out) {
+    const long long n = n_rows * d4;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long row = i / d4;
+        const int c4 = (int)(i - row * d4);
+        const float a = __ldg(lse_a + row), b = __ldg(lse_b + row);
+        float wa, wb, lse;
+        if (a == ninf() && b == ninf()) {
+            wa = 0.f;
+            wb = 0.f;
+            lse = ninf();
+        } else {
+            const float m = fmaxf(a, b);
+            const float ea = ex2((a - m) * kLog2eF), eb = ex2((b - m) * kLog2eF);
+            const float s = ea + eb;
+            wa = ea / s;
+            wb = eb / s;
+            lse = m + lg2(s) * kLn2F;
+        }
+        const float4 x = __ldg(reinterpret_cast<const float4*>(o_a) + i);
+        const float4 y = __ldg(reinterpret_cast<const float4*>(o_b) + i);
+        const uint2 out = make_uint2(pack_bf16x2(wa * x.x + wb * y.x, wa * x.y + wb * y.y),
+                                     pack_bf16x2(wa * x.z + wb * y.z, wa * x.w + wb * y.w));
+        reinterpret_cast<uint2*>(o_out)[i] = out;
+        if (c4 == 0) lse_out[row] = lse;
+    }
+}
+
+// Pass B ("Cascade attention" page, second segment): virtual request
+// v = b*topk + k attends only its own S draft tokens, draft s seeing drafts
+// 0..s.  One warp per (v, query head): each lane holds 4 of the 128 head
+// dimensions, scores are reduced across the warp with shuffles, and the
+// softmax runs online (running max, rescaled sum and accumulator) over the
+// visible drafts.
+__global__ void __launch_bounds__(256) pass_b_kernel(PassBParams p) {
+    const int warp_global = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int n_warps = p.B * p.topk * p.H_q;
+    if (warp_global >= n_warps) return;
+    const int v = warp_global / p.H_q;
+    const int hq = warp_global % p.H_q;
+    const int hk = hq / (p.H_q / p.H_kv);
+    const int32_t* trow = p.dtab + (size_t)v * p.dtab_stride;
+    for (int s = 0; s < p.S; ++s) {
+        const size_t qoff = ((size_t)(v * p.S + s) * p.H_q + hq) * 128 + lane * 4;
+        const uint2 qraw = __ldg(reinterpret_cast<const uint2*>(p.q + qoff));
+        const float q0 = __uint_as_float(qraw.x << 16), q1 = __uint_as_float(qraw.x & 0xFFFF0000u);
+        const float q2 = __uint_as_float(qraw.y << 16), q3 = __uint_as_float(qraw.y & 0xFFFF0000u);
+        float m = ninf(), l = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int j = 0; j <= s; ++j) {
+            const int pg = __ldg(trow + j / p.P);
+            if (pg < 0 || pg >= p.num_pages) {
+                if (lane == 0) atomicOr(p.status, CPA_DEV_BAD_PAGE);
+                continue;
+            }
+            const size_t off = (((size_t)pg * p.P + (j % p.P)) * p.H_kv + hk) * 128 + lane * 4;
+            const uint2 kr = __ldg(reinterpret_cast<const uint2*>(p.k_pages + off));
+            const uint2 vr = __ldg(reinterpret_cast<const uint2*>(p.v_pages + off));
+            float dot = q0 * __uint_as_float(kr.x << 16) + q1 * __uint_as_float(kr.x & 0xFFFF0000u) +
+                        q2 * __uint_as_float(kr.y << 16) + q3 * __uint_as_float(kr.y & 0xFFFF0000u);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            const float x = dot * p.scale_log2;
+            const float m_new = fmaxf(m, x);
+            const float c = ex2(m - m_new);  // 0 when m is -inf
+            const float e = ex2(x - m_new);
+            l = l * c + e;
+            a0 = a0 * c + e * __uint_as_float(vr.x << 16);
+            a1 = a1 * c + e * __uint_as_float(vr.x & 0xFFFF0000u);
+            a2 = a2 * c + e * __uint_as_float(vr.y << 16);
+            a3 = a3 * c + e * __uint_as_float(vr.y & 0xFFFF0000u);
+            m = m_new;
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        reinterpret_cast<float4*>(p.o_b + qoff)[0] = make_float4(a0 * inv, a1 * inv, a2 * inv, a3 * inv);
+        if (lane == 0)
+            p.lse_b[(size_t)(v * p.S + s) * p.H_q + hq] = l > 0.f ? (m + lg2(l)) * kLn2F : ninf();
+    }
+}
+
+// Waits on a barrier that nothing completes; the bounded wait gives up after
+// `limit_ns`, records CPA_DEV_TIMEOUT and the kernel returns normally.
+__global__ void wait_timeout_kernel(uint32_t* status, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, status, limit_ns);
+}
+
+cudaError_t launch_merge_state(const float* o_a, const float* lse_a, const float* o_b,
+                               const float* lse_b, long long n_rows, int head_dim, void* o_out,
+                               float* lse_out, int n_sm, cudaStream_t stream) {
+    const int d4 = head_dim / 4;
+    const long long n = n_rows * d4;
+    long long blocks = (n + 255) / 256;
+    const long long cap = (long long)n_sm * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    merge_state_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        o_a, lse_a, o_b, lse_b, n_rows, d4, static_cast<__nv_bfloat16*>(o_out), lse_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pass_b(const PassBParams& p, cudaStream_t stream) {
+    const long long warps = (long long)p.B * p.topk * p.H_q;
+    const long long blocks = (warps + 7) / 8;
+    pass_b_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout(uint32_t* status, unsigned long long limit_ns,
+                                cudaStream_t stream) {
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace cpa
