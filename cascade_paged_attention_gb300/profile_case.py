@@ -1,0 +1,92 @@
+"""Run one entry point of libcpa.so on a named workload, for profiling.
+
+    python -m cascade_paged_attention_gb300.profile_case --case cascade \
+        --config pages_example --warmup 2 --iters 3
+
+Generates the seeded workload, runs `warmup` untimed and `iters` timed calls
+on the current stream and prints the mean time per call (CUDA events).  Meant
+to be wrapped by ncu (one kernel name, a few launches).
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import numpy as np
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+import cascade_paged_attention_gb300 as cpa  # noqa: E402
+import cpa_synth  # noqa: E402
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", choices=["cascade", "naive", "pass_a", "pass_b", "prefill"],
+                    default="cascade")
+    ap.add_argument("--config", default="pages_example")
+    ap.add_argument("--hit", type=float, default=0.5, help="prefill: cached fraction h")
+    ap.add_argument("--batch", type=int, default=0, help="override B")
+    ap.add_argument("--warmup", type=int, default=2)
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args()
+
+    cpa.build_library()
+    dev = torch.device("cuda:0")
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(dev)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    if args.case == "prefill":
+        c = dict(cpa_synth.PREFILL_CONFIG)
+        c.pop("hits")
+        if args.batch:
+            c["B"] = args.batch
+        H = int(args.hit * c["N"])
+        wl = cpa_synth.make_prefill(H=H, **c)
+        q, kp, vp, pt = bf(wl.q), bf(wl.k_pages), bf(wl.v_pages), i32(wl.page_table)
+
+        def call():
+            cpa.cpa_prefill_hit(q, kp, vp, pt, wl.B, wl.N, wl.H)
+        work = f"prefill B={wl.B} N={wl.N} H={wl.H}: {wl.visible_pairs() * wl.B * wl.H_q} pairs"
+    else:
+        cfg = dict(cpa_synth.VERIFY_CONFIGS[args.config])
+        if args.batch:
+            cfg["B"] = args.batch
+        wl = cpa_synth.make_verify(**cfg)
+        q, kp, vp = bf(wl.q), bf(wl.k_pages), bf(wl.v_pages)
+        ppt, dpt, lens = i32(wl.prefix_page_table), i32(wl.draft_page_table), i32(wl.prefix_lens)
+        mpl = wl.max_prefix_len
+
+        def call():
+            if args.case == "cascade":
+                cpa.cpa_cascade_verify(q, kp, vp, ppt, dpt, lens, wl.topk, wl.S, mpl)
+            elif args.case == "naive":
+                cpa.cpa_naive_expand_verify(q, kp, vp, ppt, dpt, lens, wl.topk, wl.S, mpl)
+            elif args.case == "pass_a":
+                cpa.cpa_cascade_pass_a(q, kp, vp, ppt, lens, wl.topk, wl.S, mpl)
+            else:
+                cpa.cpa_cascade_pass_b(q, kp, vp, dpt, wl.B, wl.topk, wl.S)
+        work = (f"{args.config}: unique KV {wl.unique_kv_tokens() * wl.kv_bytes_per_token() / 1e6:.1f}"
+                f" MB")
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.iters):
+        call()
+    e.record()
+    torch.cuda.synchronize()
+    print(f"{args.case} {work}: {s.elapsed_time(e) / args.iters * 1e3:.1f} us/call")
+
+
+if __name__ == "__main__":
+    main()
