@@ -45,6 +45,21 @@ constexpr float kRescaleLog2 = 8.0f;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// Timestamps of pipeline events for a few CTAs, only in builds that define
+// CPA_TRACE (a diagnostic build provides the buffer); otherwise no code.
+#ifdef CPA_TRACE
+static __device__ unsigned long long* cpa_trace_buf = nullptr;
+#define CPA_TRACE_EVENT(ev, idx)                                                  \
+    do {                                                                          \
+        if (cpa_trace_buf && blockIdx.x < 4 && (idx) < 1024)                      \
+            cpa_trace_buf[(blockIdx.x * 16 + (ev)) * 1024 + (idx)] = clock64();   \
+    } while (0)
+#else
+#define CPA_TRACE_EVENT(ev, idx) \
+    do {                         \
+    } while (0)
+#endif
+
 struct AttnParams {
     CUtensorMap qmap;
     CUtensorMap kmap;
@@ -447,6 +462,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                        abort_flag, p.status);
                         if (!ok) break;
                     }
+                    if (lane == 0) CPA_TRACE_EVENT(0, g);
                     const int box0 = jj * NB;
                     if (box0 >= wbase + 32) {
                         cur = nxt;
@@ -517,6 +533,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                        abort_flag, p.status))
                             return false;
                     }
+                    CPA_TRACE_EVENT(3, pg_);
                     tc_fence_after_sync();
                     const uint32_t vb = sbase + p.off_kv + pst * kStageBytes + 2 * kBN * 128;
                     for (int mt = 0; mt < NUM_MT; ++mt) {
@@ -549,6 +566,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         ok = mbar_wait(&ctrl->kv_full[st], (uint32_t)((g / p.n_stages) & 1),
                                        abort_flag, p.status);
                         if (!ok) break;
+                        CPA_TRACE_EVENT(2, g);
                         tc_fence_after_sync();
                         const int sb = (int)(g & 1);
                         const uint32_t kb = sbase + p.off_kv + st * kStageBytes;
@@ -612,6 +630,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     ok = mbar_wait_warp(&ctrl->s_full[g & 1], (uint32_t)((g >> 1) & 1), abort_flag,
                                    p.status);
                     if (!ok) break;
+                    if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(4, g);
                     tc_fence_after_sync();
                     uint32_t sr[64];
                     tmem_ld_x64(tmem + lane_addr + C::s_col(mt, (int)(g & 1)), sr);
@@ -660,6 +679,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         pk[c] = pack_bf16x2(a, b);
                     }
                     l += sum;
+                    if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(5, g);
                     // the P buffer this tile writes must no longer be read by an earlier PV
                     if (C::kPBufs == 2) {
                         if (g >= 2)
@@ -692,6 +712,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     fence_proxy_async_smem();
                     tc_fence_before_sync();
                     mbar_arrive(&ctrl->p_full[g & 1]);
+                    if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(6, g);
                 }
                 if (!ok) break;
                 if (w.seg >= C::kOBufs) {
@@ -728,6 +749,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                      mbar_wait(&ctrl->stats_full[ob], ph, abort_flag, p.status);
                 ok = bar_and(1, 128, ok);  // one decision for the whole epilogue warpgroup
                 if (!ok) break;
+                if (et == 0) CPA_TRACE_EVENT(7, w.seg);
                 tc_fence_after_sync();
 
                 // stage this unit's draft K/V rows (verify) in shared memory
@@ -968,6 +990,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         if (verify_out) named_bar_sync(1, 128);
                     }
                 }
+                if (et == 0) CPA_TRACE_EVENT(8, w.seg);
                 w.next(x, jb, je);
             }
         }
