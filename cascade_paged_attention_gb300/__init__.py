@@ -25,6 +25,7 @@ __all__ = [
     "cpa_prefill_hit_workspace_size",
     "cpa_status_workspace_size",
     "cpa_cascade_verify",
+    "cpa_cascade_verify_noalloc",
     "cpa_naive_expand_verify",
     "cpa_cascade_pass_a",
     "cpa_cascade_pass_b",
@@ -84,6 +85,7 @@ def lib() -> ctypes.CDLL:
         "cpa_prefill_hit_workspace_size": (SZ, [I, I, I, I, I, I, I]),
         "cpa_cascade_verify": (I, verify_args),
         "cpa_naive_expand_verify": (I, verify_args),
+        "cpa_cascade_verify_noalloc": (I, verify_args[:20] + [P]),
         "cpa_cascade_pass_a": (I, [P, P, P, P, I, P, I, I, I, I, I, I, I, I, I, F, P, P, P, SZ,
                                    P]),
         "cpa_cascade_pass_b": (I, [P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
@@ -227,6 +229,37 @@ def cpa_cascade_verify(q, k_pages, v_pages, prefix_page_table, draft_page_table,
     return _verify_call("cpa_cascade_verify", q, k_pages, v_pages, prefix_page_table,
                         draft_page_table, prefix_lens, topk, S, max_prefix_len, sm_scale, o, lse,
                         workspace, stream)
+
+
+def cpa_cascade_verify_noalloc(q, k_pages, v_pages, prefix_page_table, draft_page_table,
+                               prefix_lens, topk: int, S: int, o, lse,
+                               max_prefix_len: Optional[int] = None,
+                               sm_scale: Optional[float] = None, stream=None):
+    """Cascade verify without a workspace, for callers that cannot allocate device memory.
+
+    The library keeps its scratch in a fixed-size array it owns on every GPU,
+    and this path allocates nothing: the caller passes preallocated `o`
+    (bf16, shaped like q) and `lse` (fp32 [T, H_q]).  Returns (o, lse).
+    """
+    B, H_q, H_kv, d, P, num_pages = _verify_shapes(q, k_pages, v_pages, prefix_page_table,
+                                                    prefix_lens, topk, S)
+    _need(draft_page_table, "draft_page_table", torch.int32, 2)
+    _need(o, "o", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    if draft_page_table.shape[0] != B * topk or o.shape != q.shape or \
+            lse.shape != (q.shape[0], H_q):
+        raise ValueError("inconsistent verify shapes")
+    if max_prefix_len is None:
+        max_prefix_len = prefix_page_table.shape[1] * P
+    if sm_scale is None:
+        sm_scale = d ** -0.5
+    st = lib().cpa_cascade_verify_noalloc(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(prefix_page_table),
+        prefix_page_table.shape[1], _ptr(draft_page_table), draft_page_table.shape[1],
+        _ptr(prefix_lens), B, topk, S, H_q, H_kv, d, P, num_pages, int(max_prefix_len),
+        float(sm_scale), _ptr(o), _ptr(lse), _stream(stream))
+    _check("cpa_cascade_verify_noalloc", st)
+    return o, lse
 
 
 def cpa_naive_expand_verify(q, k_pages, v_pages, prefix_page_table, draft_page_table,

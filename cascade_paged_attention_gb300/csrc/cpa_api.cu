@@ -487,3 +487,57 @@ int cpa_plan_partition(int64_t total, int n_ctas, int cta, int64_t tile, int64_t
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Static-scratch variant: the workspace is a file-scope device array, so this
+// path allocates nothing.  Host code never passes g_static_scratch itself (in
+// host code the name stands for a host-side shadow); it resolves the device
+// address once per device with cudaGetSymbolAddress.
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[CPA_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+void* static_scratch_for_current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+        g_scratch_ptr[dev] = p;
+    }
+    return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+cpa_status cpa_cascade_verify_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                      const int32_t* prefix_page_table, int prefix_pt_stride,
+                                      const int32_t* draft_page_table, int draft_pt_stride,
+                                      const int32_t* prefix_lens, int B, int topk, int S, int H_q,
+                                      int H_kv, int head_dim, int page_size, int num_pages,
+                                      int max_prefix_len, float sm_scale, void* o, float* lse,
+                                      cpa_stream_t stream) {
+    const size_t need =
+        cpa_cascade_verify_workspace_size(B, topk, S, H_q, H_kv, head_dim, page_size);
+    void* scratch = nullptr;
+    if (need != 0) {
+        if (need > (size_t)CPA_STATIC_SCRATCH_BYTES) return CPA_ERR_WORKSPACE;
+        scratch = static_scratch_for_current_device();
+        if (!scratch) return CPA_ERR_CUDA;
+    }
+    // need == 0: the sizes are invalid; the shared checks report which error.
+    return verify_common(MODE_CASCADE, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                         draft_page_table, draft_pt_stride, prefix_lens, B, topk, S, H_q, H_kv,
+                         head_dim, page_size, num_pages, max_prefix_len, sm_scale, o, lse,
+                         scratch, scratch ? (size_t)CPA_STATIC_SCRATCH_BYTES : 0,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

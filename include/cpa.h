@@ -241,6 +241,39 @@ cpa_status cpa_debug_wait_timeout(void* workspace, size_t workspace_bytes, int l
 int cpa_plan_partition(int64_t total, int n_ctas, int cta, int64_t tile, int64_t* begin,
                        int64_t* end);
 
+/*
+ * Static-scratch cascade verify: the same computation, arguments and
+ * results as cpa_cascade_verify, but no workspace argument and no
+ * allocation by anyone.  The source pages have no counterpart of this call;
+ * it exists for callers that cannot call cudaMalloc.  Examples: an inference
+ * engine that reserves nearly all HBM for its paged KV pool at start-up and
+ * forbids later driver allocations (they would fail or fragment the pool);
+ * a latency-critical decode loop that cannot pay for cudaMalloc's implicit
+ * device-wide synchronisation; plugin code hosted by a framework that owns
+ * every device buffer and hands the plugin no allocator.
+ *
+ * Scratch: a file-scope device array of CPA_STATIC_SCRATCH_BYTES, which every
+ * GPU that loads this library holds until the process exits.  Sizes whose
+ * workspace (cpa_cascade_verify_workspace_size) exceeds it are rejected with
+ * CPA_ERR_WORKSPACE before anything is launched.  The first call on a device,
+ * with that device current, looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls on a device share the one array and it keeps the last call's
+ * contents: each call clears the status word and merge counters it needs
+ * (asynchronous memset on `stream`) before its kernel runs.  Calls that
+ * overlap on the GPU (different streams, no ordering between them) race on
+ * the array.
+ */
+#define CPA_STATIC_SCRATCH_BYTES (48u * 1024u * 1024u)
+
+cpa_status cpa_cascade_verify_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                      const int32_t* prefix_page_table, int prefix_pt_stride,
+                                      const int32_t* draft_page_table, int draft_pt_stride,
+                                      const int32_t* prefix_lens, int B, int topk, int S, int H_q,
+                                      int H_kv, int head_dim, int page_size, int num_pages,
+                                      int max_prefix_len, float sm_scale, void* o, float* lse,
+                                      cpa_stream_t stream);
+
 /* Library version, e.g. 100 for 0.1.0. */
 int cpa_version(void);
 
