@@ -89,11 +89,14 @@ struct Geometry {
     int num_mt;
     int TS, TSB, Rq;
     int n_stages, n_qbufs;
-    uint32_t off_q, off_kv, off_p, off_draft;
+    uint32_t off_q, off_kv;
     int smem_bytes;
 };
 
-bool plan_geometry(int G, int TS, bool draft, bool prefill, Geometry& g) {
+// Shared-memory plan: control block and row statistics, Q buffers, then the
+// K/V stage ring.  As many stages as fit (up to 6), Q double-buffered when a
+// unit has a single M tile.
+bool plan_geometry(int G, int TS, Geometry& g) {
     const int rows = TS * G;
     if (rows <= 0 || rows > kMaxUnitRows) return false;
     g.num_mt = rows <= 128 ? 1 : 2;
@@ -102,26 +105,17 @@ bool plan_geometry(int G, int TS, bool draft, bool prefill, Geometry& g) {
     const int rows_mt = G * g.TSB;
     if (rows_mt > 128) return false;
     g.Rq = (rows_mt + 7) / 8 * 8;
-    const int pbufs = g.num_mt == 1 ? 2 : 1;
     const size_t qmt = (size_t)2 * g.Rq * 128;
-    const int tries[5][2] = {{4, 2}, {4, 1}, {3, 2}, {3, 1}, {2, 1}};
-    for (int t = 0; t < 5; ++t) {
-        int st = tries[t][0], qb = tries[t][1];
-        if (g.num_mt == 2 && qb == 2) continue;
-        if (prefill && st == 4 && qb == 2) continue;  // prefer Q double-buffering at 3 stages
-        size_t off_q = kOffData;
-        size_t off_kv = align_up(off_q + (size_t)qb * g.num_mt * qmt, 1024);
-        size_t off_p = off_kv + (size_t)st * kStageBytes;
-        size_t off_d = off_p + (size_t)g.num_mt * pbufs * kPBytes;
-        size_t end = off_d + (draft ? (size_t)kMaxDraftKeys * 512 : 0);
-        size_t total = end + 1024;
+    const int qb = g.num_mt == 1 ? 2 : 1;
+    const size_t off_q = kOffData;
+    const size_t off_kv = align_up(off_q + (size_t)qb * g.num_mt * qmt, 1024);
+    for (int st = 6; st >= 2; --st) {
+        const size_t total = off_kv + (size_t)st * kStageBytes + 1024;
         if (total <= (size_t)kMaxSmemOptin) {
             g.n_stages = st;
             g.n_qbufs = qb;
             g.off_q = (uint32_t)off_q;
             g.off_kv = (uint32_t)off_kv;
-            g.off_p = (uint32_t)off_p;
-            g.off_draft = (uint32_t)off_d;
             g.smem_bytes = (int)total;
             return true;
         }
@@ -165,8 +159,6 @@ cpa_status run_attn(AttnParams& p, const Geometry& geo, long long n_units, void*
     p.n_qbufs = geo.n_qbufs;
     p.off_q = geo.off_q;
     p.off_kv = geo.off_kv;
-    p.off_p = geo.off_p;
-    p.off_draft = geo.off_draft;
     if (cudaMemsetAsync(workspace, 0, wl.part_lse, stream) != cudaSuccess) return CPA_ERR_CUDA;
     cudaError_t e = geo.num_mt == 1 ? launch_attn<1>(p, geo.smem_bytes, n_sm, stream)
                                     : launch_attn<2>(p, geo.smem_bytes, n_sm, stream);
@@ -182,7 +174,7 @@ cpa_status check_verify(const void* q, const void* k_pages, const void* v_pages,
     if (B < 1 || topk < 1 || S < 1 || H_q < 1 || H_kv < 1 || num_pages < 1 || max_prefix_len < 0)
         return CPA_ERR_INVALID_ARG;
     if (H_q % H_kv != 0) return CPA_ERR_INVALID_ARG;
-    if (!std::isfinite(sm_scale)) return CPA_ERR_INVALID_ARG;
+    if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return CPA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages)) return CPA_ERR_INVALID_ARG;
     if (head_dim != 128) return CPA_ERR_UNSUPPORTED;
     if (!page_size_ok(page_size)) return CPA_ERR_UNSUPPORTED;
@@ -239,26 +231,37 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
     if (st != CPA_OK) return st;
     if (!o || !lse || !aligned16(o)) return CPA_ERR_INVALID_ARG;
     const bool draft = mode != MODE_PASS_A;
+    // The draft tile holds each branch's drafts in a block of sb rows, all read
+    // from the branch's first draft page.
+    const int sb = S <= 8 ? 8 : 16;
+    const int nbr = mode == MODE_CASCADE ? topk : 1;
     if (draft) {
         if (!dpt || dpt_stride < (S + page_size - 1) / page_size) return CPA_ERR_INVALID_ARG;
-        if (S > kMaxDraft) return CPA_ERR_UNSUPPORTED;
+        if (S > kMaxDraft || S > page_size || nbr * sb > kBN) return CPA_ERR_UNSUPPORTED;
     }
     const int G = H_q / H_kv;
     const int TS = mode == MODE_NAIVE ? S : topk * S;
-    if (draft && TS > kMaxDraftKeys) return CPA_ERR_UNSUPPORTED;
     Geometry geo;
-    if (!plan_geometry(G, TS, draft, false, geo)) return CPA_ERR_UNSUPPORTED;
+    if (!plan_geometry(G, TS, geo)) return CPA_ERR_UNSUPPORTED;
     AttnParams p;
     fill_common(p, q, k_pages, v_pages, ppt, ppt_stride, dpt, dpt_stride, lens, B, topk, S, H_q,
                 H_kv, page_size, num_pages, max_prefix_len, sm_scale);
     p.mode = mode;
     p.upg = mode == MODE_NAIVE ? topk * H_kv : H_kv;
-    p.draft_keys = draft ? TS : 0;
+    p.has_draft = draft ? 1 : 0;
+    p.sb = sb;
+    p.nbr = nbr;
     p.o = o;
     p.lse = lse;
     const uint64_t T = (uint64_t)B * topk * S;
     if (!make_map(&p.qmap, q, H_q, T, G, geo.TSB)) return CPA_ERR_CUDA;
     if (!kv_maps(p, k_pages, v_pages, H_kv, num_pages, page_size)) return CPA_ERR_CUDA;
+    if (draft) {
+        const uint64_t rows = (uint64_t)num_pages * page_size;
+        if (!make_map(&p.kdmap, k_pages, H_kv, rows, 1, sb) ||
+            !make_map(&p.vdmap, v_pages, H_kv, rows, 1, sb))
+            return CPA_ERR_CUDA;
+    }
     const long long n_units = (long long)B * p.upg;
     return run_attn(p, geo, n_units, workspace, ws_bytes, stream);
 }
@@ -414,7 +417,7 @@ cpa_status cpa_prefill_hit(const void* q, const void* k_pages, const void* v_pag
                            size_t workspace_bytes, cpa_stream_t stream) {
     if (!q || !k_pages || !v_pages || !page_table || !o || !lse) return CPA_ERR_INVALID_ARG;
     if (B < 1 || N < 1 || H_hit < 0 || H_hit > N || H_q < 1 || H_kv < 1 || H_q % H_kv ||
-        num_pages < 1 || !std::isfinite(sm_scale))
+        num_pages < 1 || !(sm_scale > 0.f) || !std::isfinite(sm_scale))
         return CPA_ERR_INVALID_ARG;
     if (part != CPA_PREFILL_FULL && part != CPA_PREFILL_RECT && part != CPA_PREFILL_TRI)
         return CPA_ERR_INVALID_ARG;
@@ -429,7 +432,7 @@ cpa_status cpa_prefill_hit(const void* q, const void* k_pages, const void* v_pag
     if (M == 0) return CPA_OK;
     const int TS = 128 / G;
     Geometry geo;
-    if (!plan_geometry(G, TS, false, true, geo)) return CPA_ERR_UNSUPPORTED;
+    if (!plan_geometry(G, TS, geo)) return CPA_ERR_UNSUPPORTED;
     AttnParams p;
     fill_common(p, q, k_pages, v_pages, page_table, pt_stride, nullptr, 0, nullptr, B, 1, 1, H_q,
                 H_kv, page_size, num_pages, 0, sm_scale);

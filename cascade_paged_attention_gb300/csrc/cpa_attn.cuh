@@ -24,11 +24,17 @@
 //   w = 1      MMA issuer: S = Q K^T (M=128, N=64, K=128) into TMEM, then
 //              O += P V (M=128, N=128, K=64) into TMEM;
 //   w = 4..    softmax, one warpgroup per 128-row M tile: reads its S row
-//              from TMEM, masks, exponentiates (base 2), writes bf16 P into
-//              swizzled shared memory, and rescales O in TMEM only when the
-//              running max grew by more than 2^8;
-//   last 4     epilogue: O / l, split-piece merge, then (verify) the row's
-//              own-branch draft attention and the final merge, bf16 store.
+//              from TMEM, masks, exponentiates (base 2), writes bf16 P back
+//              over the S columns it came from (the PV MMA reads P from
+//              TMEM), and rescales O in TMEM only when the running max grew
+//              by more than 2^8.  On a unit's last tile (its drafts, or the
+//              causal diagonal) it also writes the bf16 residual of P, and PV
+//              runs twice, so rows that see few keys keep P to ~16 bits;
+//   last 4     epilogue: O / l, the merge of units split across CTAs, store.
+// Verify units end with one extra tile holding the unit's own draft tokens
+// (Pass B): branch k's drafts fill rows k*sb.. of that tile and the softmax
+// applies the causal-within-branch mask, so Pass B and its merge with Pass A
+// run inside the same online softmax on the tensor cores.
 // O is double-buffered in TMEM for one M tile, so the epilogue of one unit
 // overlaps the next unit's main loop.
 #pragma once
@@ -64,6 +70,8 @@ struct AttnParams {
     CUtensorMap qmap;
     CUtensorMap kmap;
     CUtensorMap vmap;
+    CUtensorMap kdmap;  // K/V pool with draft-block boxes (sb rows)
+    CUtensorMap vdmap;
     const __nv_bfloat16* q;
     const __nv_bfloat16* k_pages;
     const __nv_bfloat16* v_pages;
@@ -86,9 +94,11 @@ struct AttnParams {
     int Rq;               // rows of one Q M-tile buffer (multiple of 8)
     int boxr;             // rows of one K/V TMA box
     int n_stages, n_qbufs;
-    int draft_keys;       // draft keys staged per unit (cascade topk*S, naive S)
+    int has_draft;        // cascade / naive: the unit's drafts form its last tile
+    int sb;               // rows per branch block in the draft tile (8 or 16)
+    int nbr;              // branches per unit (cascade topk, naive 1)
     float scale_log2;     // sm_scale * log2(e)
-    uint32_t off_q, off_kv, off_p, off_draft;
+    uint32_t off_q, off_kv;
 };
 
 // ------------------------------------------------------------------ units
@@ -100,6 +110,7 @@ struct Unit {
     int lo, hi;       // keys [lo, hi) visible (prefill full/tri: hi of the last row)
     int valid_end;    // keys at or past this are not in the sequence
     int tile_base;    // first key tile
+    int n_prefix;     // prefix tiles; tile n_prefix (verify) holds the unit's drafts
     int n_tiles;
     const int32_t* trow;
 };
@@ -138,6 +149,17 @@ __device__ __forceinline__ int prefill_qt_tiles(const AttnParams& p, int qt) {
     return tiles_for(lo, hi);
 }
 
+// Tiles of one verify unit with prefix length L: the prefix tiles, then (for
+// cascade / naive) one tile holding the unit's own draft tokens.  A unit
+// always has at least one tile, so every row gets an output.
+__device__ __forceinline__ int verify_prefix_tiles(const AttnParams& p, int L) {
+    const int t = (L + kBN - 1) / kBN;
+    return p.has_draft ? t : (t < 1 ? 1 : t);
+}
+__device__ __forceinline__ int verify_unit_tiles(const AttnParams& p, int L) {
+    return verify_prefix_tiles(p, L) + (p.has_draft ? 1 : 0);
+}
+
 __device__ __forceinline__ Unit get_unit(const AttnParams& p, int u) {
     Unit x;
     if (is_verify(p.mode)) {
@@ -148,7 +170,8 @@ __device__ __forceinline__ Unit get_unit(const AttnParams& p, int u) {
         x.hi = L;
         x.valid_end = L;
         x.tile_base = 0;
-        x.n_tiles = L > 0 ? (L + kBN - 1) / kBN : 1;
+        x.n_prefix = verify_prefix_tiles(p, L);
+        x.n_tiles = verify_unit_tiles(p, L);
         x.p0 = 0;
         x.trow = p.ptab + (size_t)b * p.ptab_stride;
         if (p.mode == MODE_NAIVE) {
@@ -175,6 +198,7 @@ __device__ __forceinline__ Unit get_unit(const AttnParams& p, int u) {
         prefill_keys(p, x.p0, x.ntok, x.lo, x.hi);
         x.tile_base = x.lo / kBN;
         x.n_tiles = tiles_for(x.lo, x.hi);
+        x.n_prefix = x.n_tiles;
         x.trow = p.ptab + (size_t)x.b * p.ptab_stride;
     }
     return x;
@@ -182,7 +206,7 @@ __device__ __forceinline__ Unit get_unit(const AttnParams& p, int u) {
 
 // ------------------------------------------------------------------ shared control block
 struct Ctrl {
-    uint64_t kv_full[4], kv_empty[4];
+    uint64_t kv_full[6], kv_empty[6];
     uint64_t q_full[2], q_empty[2];
     uint64_t s_full[2], p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2], stats_full[2];
@@ -204,11 +228,9 @@ static_assert(sizeof(Ctrl) <= 1024, "control block");
 constexpr uint32_t kOffStats = 1024;  // float2 [2][256] of (max, sum) per row: 4 KB
 constexpr uint32_t kOffData = 5120;   // first 1024-aligned byte after the stats
 constexpr uint32_t kStageBytes = 4u * kBN * 128u;
-constexpr uint32_t kPBytes = 128u * 128u;
 
 template <int NUM_MT>
 struct Cfg {
-    static constexpr int kPBufs = NUM_MT == 1 ? 2 : 1;
     static constexpr int kOBufs = NUM_MT == 1 ? 2 : 1;
     static constexpr int kSmWarp0 = 4;
     static constexpr int kEpiWarp0 = 4 + 4 * NUM_MT;
@@ -261,8 +283,7 @@ __device__ __forceinline__ void schedule(const AttnParams& p, Ctrl* c) {
             if (b < p.B) {
                 const int L = __ldg(p.lens + b);
                 if (L < 0 || L > p.max_len) atomicOr(p.status, CPA_DEV_BAD_LENGTH);
-                const int Lc = prefix_len(p, b);
-                v = (long long)p.upg * (Lc > 0 ? (Lc + kBN - 1) / kBN : 1);
+                v = (long long)p.upg * verify_unit_tiles(p, prefix_len(p, b));
             }
             long long tot;
             block_scan(v, c->scan, tot);
@@ -297,8 +318,7 @@ __device__ __forceinline__ void schedule(const AttnParams& p, Ctrl* c) {
             long long v = 0;
             int tpu = 1;
             if (b < p.B) {
-                const int Lc = prefix_len(p, b);
-                tpu = Lc > 0 ? (Lc + kBN - 1) / kBN : 1;
+                tpu = verify_unit_tiles(p, prefix_len(p, b));
                 v = (long long)p.upg * tpu;
             }
             long long tot;
@@ -362,6 +382,34 @@ struct Walker {
     }
 };
 
+// A tile-by-tile cursor over this CTA's range: the unit, the tile within it,
+// and whether the tile opens or closes this CTA's piece of the unit.
+struct TileCursor {
+    Walker w;
+    Unit x;
+    int jb, je, jj;
+    __device__ __forceinline__ void init(const Ctrl* c, const AttnParams& p) {
+        w.init(c);
+        if (w.left > 0) {
+            x = get_unit(p, w.u);
+            w.piece(x, jb, je);
+            jj = jb;
+        }
+    }
+    __device__ __forceinline__ bool first() const { return jj == jb; }
+    __device__ __forceinline__ bool last() const { return jj == je - 1; }
+    __device__ __forceinline__ void advance(const AttnParams& p) {
+        if (++jj == je) {
+            w.next(x, jb, je);
+            if (w.left > 0) {
+                x = get_unit(p, w.u);
+                w.piece(x, jb, je);
+                jj = jb;
+            }
+        }
+    }
+};
+
 // ------------------------------------------------------------------ epilogue helpers
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -381,7 +429,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     volatile uint32_t* abort_flag = &ctrl->abort_flag;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 6; ++i) {
             mbar_init(&ctrl->kv_full[i], 1);
             mbar_init(&ctrl->kv_empty[i], 1);
         }
@@ -455,12 +503,41 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 int wbase = jb * NB;
                 int cur = load_page(wbase + lane);
                 int nxt = load_page(wbase + 32 + lane);
+                // first draft page of branch lane/4, if this piece ends with the draft tile
+                int dpage = -1;
+                if (p.has_draft && je == x.n_tiles && (lane >> 2) < p.nbr)
+                    dpage = __ldg(p.dtab + (size_t)(x.b * p.topk + x.branch0 + (lane >> 2)) *
+                                               p.dtab_stride);
                 for (int jj = jb; jj < je; ++jj, ++g) {
                     const int st = (int)(g % p.n_stages);
                     if (g >= p.n_stages) {
                         ok = mbar_wait_warp(&ctrl->kv_empty[st], (uint32_t)(((g / p.n_stages) - 1) & 1),
                                        abort_flag, p.status);
                         if (!ok) break;
+                    }
+                    if (jj >= x.n_prefix) {
+                        // the unit's draft tile: branch k's drafts 0..S-1 sit in slots
+                        // 0..S-1 of its first draft page; lane 4k+part loads one
+                        // sb-row box (K lo/hi, V lo/hi) into rows k*sb.. of the tile
+                        if (lane == 0) CPA_TRACE_EVENT(0, g);
+                        const int k = lane >> 2, part = lane & 3;
+                        bool use = k < p.nbr;
+                        if (use && (dpage < 0 || dpage >= p.num_pages)) {
+                            if (part == 0) atomicOr(p.status, CPA_DEV_BAD_PAGE);
+                            use = false;
+                        }
+                        const uint32_t mask = __ballot_sync(0xffffffffu, use);
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(&ctrl->kv_full[st],
+                                                  (uint32_t)__popc(mask) * p.sb * 128u);
+                        __syncwarp();
+                        if (use) {
+                            uint8_t* dst = smem + p.off_kv + st * kStageBytes + part * (kBN * 128) +
+                                           k * p.sb * 128;
+                            tma_load_3d(dst, part < 2 ? &p.kdmap : &p.vdmap, (part & 1) * 64, x.h,
+                                        dpage * p.P, &ctrl->kv_full[st], pol_kv);
+                        }
+                        continue;
                     }
                     if (lane == 0) CPA_TRACE_EVENT(0, g);
                     const int box0 = jj * NB;
@@ -482,21 +559,20 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         const uint32_t bytes = (uint32_t)__popc(mask) * 4u * p.boxr * 128u;
                         mbar_arrive_expect_tx(&ctrl->kv_full[st], bytes);
                     }
-                    uint8_t* sk = smem + p.off_kv + st * kStageBytes;
-                    for (int i = 0; i < NB; ++i) {
-                        const int pgi = __shfl_sync(0xffffffffu, pg, i);
-                        if (lane == 0 && (mask >> i & 1u)) {
-                            const int posi = key_base + (box0 + i) * p.boxr;
-                            const int row = pgi * p.P + (posi % p.P);
-                            uint8_t* dk = sk + i * p.boxr * 128;
-                            tma_load_3d(dk, &p.kmap, 0, x.h, row, &ctrl->kv_full[st], pol_kv);
-                            tma_load_3d(dk + kBN * 128, &p.kmap, 64, x.h, row, &ctrl->kv_full[st],
-                                        pol_kv);
-                            tma_load_3d(dk + 2 * kBN * 128, &p.vmap, 0, x.h, row,
-                                        &ctrl->kv_full[st], pol_kv);
-                            tma_load_3d(dk + 3 * kBN * 128, &p.vmap, 64, x.h, row,
-                                        &ctrl->kv_full[st], pol_kv);
-                        }
+                    // One TMA per lane: a thread issues TMA copies one after another,
+                    // so spreading the 4*NB boxes of a tile over 4*NB lanes keeps the
+                    // copy engine fed.  Lane l loads part l%4 (K lo/hi, V lo/hi
+                    // half) of box l/4.
+                    const int bi = lane >> 2, part = lane & 3;
+                    const int pgi = __shfl_sync(0xffffffffu, pg, bi & 31);
+                    __syncwarp();
+                    if (bi < NB && (mask >> bi & 1u)) {
+                        const int posi = key_base + (box0 + bi) * p.boxr;
+                        const int row = pgi * p.P + (posi % p.P);
+                        uint8_t* dst = smem + p.off_kv + st * kStageBytes + part * (kBN * 128) +
+                                       bi * p.boxr * 128;
+                        tma_load_3d(dst, part < 2 ? &p.kmap : &p.vmap, (part & 1) * 64, x.h, row,
+                                    &ctrl->kv_full[st], pol_kv);
                     }
                 }
                 w.next(x, jb, je);
@@ -512,93 +588,109 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             }
         } else if (warp == 1) {
             // ============================== MMA issuer
+            // Two cursors walk the same tile sequence: one issues S = Q K^T as soon
+            // as a tile's K/V and Q have landed, the other issues O += P V as soon
+            // as the softmax has written that tile's P.  Whichever is ready goes
+            // first, so a late K/V tile never holds back the PV that frees a stage.
             if (lane == 0) {
                 const uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
                 const uint32_t idesc_o = idesc_bf16_f32(128, 128, true);
                 const uint32_t qmt_bytes = (uint32_t)(2 * p.Rq * 128);
-                Walker w;
-                w.init(ctrl);
-                long long g = 0;
+                TileCursor cs, cp;
+                cs.init(ctrl, p);
+                cp.init(ctrl, p);
+                long long gs = 0, gp = 0;  // next tile for S / for PV
+                const long long n_tiles = ctrl->count;
+                uint64_t t_idle = 0;
+                uint32_t spins = 0;
                 bool ok = true;
-                bool have_prev = false;
-                long long pg_ = 0;
-                int pst = 0, pseg = 0, pob = 0;
-                bool pfirst = false, plast = false;
-                auto issue_pv = [&]() -> bool {
-                    if (!mbar_wait(&ctrl->p_full[pg_ & 1], (uint32_t)((pg_ >> 1) & 1), abort_flag,
-                                   p.status))
-                        return false;
-                    if (pfirst && pseg >= C::kOBufs) {
-                        if (!mbar_wait(&ctrl->o_empty[pob], ((pseg / C::kOBufs) - 1) & 1,
-                                       abort_flag, p.status))
-                            return false;
-                    }
-                    CPA_TRACE_EVENT(3, pg_);
-                    tc_fence_after_sync();
-                    const uint32_t vb = sbase + p.off_kv + pst * kStageBytes + 2 * kBN * 128;
-                    for (int mt = 0; mt < NUM_MT; ++mt) {
-                        const uint32_t pa =
-                            sbase + p.off_p + (mt * C::kPBufs + (int)(pg_ % C::kPBufs)) * kPBytes;
+                while (gp < n_tiles) {
+                    bool progressed = false;
+                    if (gs < n_tiles && gs <= gp + 1) {
+                        const int qb = cs.w.seg % p.n_qbufs;
+                        const int st = (int)(gs % p.n_stages);
+                        const bool q_ready =
+                            !cs.first() || mbar_test(&ctrl->q_full[qb], (cs.w.seg / p.n_qbufs) & 1);
+                        if (q_ready && mbar_test(&ctrl->kv_full[st], (uint32_t)((gs / p.n_stages) & 1))) {
+                            CPA_TRACE_EVENT(2, gs);
+                            tc_fence_after_sync();
+                            const int sb = (int)(gs & 1);
+                            const uint32_t kb = sbase + p.off_kv + st * kStageBytes;
+                            for (int mt = 0; mt < NUM_MT; ++mt) {
+                                const uint32_t qa = sbase + p.off_q + (qb * NUM_MT + mt) * qmt_bytes;
 #pragma unroll
-                        for (int kk = 0; kk < kBN / 16; ++kk) {
-                            const uint64_t a = sdesc_sw128(pa + kk * 32, 16, 1024);
-                            const uint64_t b = sdesc_sw128(vb + kk * 16 * 128, kBN * 128, 1024);
-                            umma_bf16_ss(tmem + C::o_col(mt, pob), a, b, idesc_o,
-                                         (pfirst && kk == 0) ? 0u : 1u);
-                        }
-                    }
-                    umma_commit(&ctrl->p_empty[pg_ & 1]);
-                    umma_commit(&ctrl->kv_empty[pst]);
-                    if (plast) umma_commit(&ctrl->o_full[pob]);
-                    return true;
-                };
-                while (w.left > 0 && ok) {
-                    const Unit x = get_unit(p, w.u);
-                    int jb, je;
-                    w.piece(x, jb, je);
-                    const int qb = w.seg % p.n_qbufs;
-                    const int ob = w.seg % C::kOBufs;
-                    ok = mbar_wait(&ctrl->q_full[qb], (w.seg / p.n_qbufs) & 1, abort_flag,
-                                   p.status);
-                    if (!ok) break;
-                    for (int jj = jb; jj < je; ++jj, ++g) {
-                        const int st = (int)(g % p.n_stages);
-                        ok = mbar_wait(&ctrl->kv_full[st], (uint32_t)((g / p.n_stages) & 1),
-                                       abort_flag, p.status);
-                        if (!ok) break;
-                        CPA_TRACE_EVENT(2, g);
-                        tc_fence_after_sync();
-                        const int sb = (int)(g & 1);
-                        const uint32_t kb = sbase + p.off_kv + st * kStageBytes;
-                        for (int mt = 0; mt < NUM_MT; ++mt) {
-                            const uint32_t qa = sbase + p.off_q + (qb * NUM_MT + mt) * qmt_bytes;
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const uint64_t a = sdesc_sw128(
-                                    qa + (kk >> 2) * p.Rq * 128 + (kk & 3) * 32, 16, 1024);
-                                const uint64_t b = sdesc_sw128(
-                                    kb + (kk >> 2) * kBN * 128 + (kk & 3) * 32, 16, 1024);
-                                umma_bf16_ss(tmem + C::s_col(mt, sb), a, b, idesc_s,
-                                             kk > 0 ? 1u : 0u);
+                                for (int kk = 0; kk < 8; ++kk) {
+                                    const uint64_t ad = sdesc_sw128(
+                                        qa + (kk >> 2) * p.Rq * 128 + (kk & 3) * 32, 16, 1024);
+                                    const uint64_t bd = sdesc_sw128(
+                                        kb + (kk >> 2) * kBN * 128 + (kk & 3) * 32, 16, 1024);
+                                    umma_bf16_ss(tmem + C::s_col(mt, sb), ad, bd, idesc_s,
+                                                 kk > 0 ? 1u : 0u);
+                                }
                             }
+                            umma_commit(&ctrl->s_full[sb]);
+                            if (cs.last()) umma_commit(&ctrl->q_empty[qb]);
+                            cs.advance(p);
+                            ++gs;
+                            progressed = true;
                         }
-                        umma_commit(&ctrl->s_full[sb]);
-                        if (jj == je - 1) umma_commit(&ctrl->q_empty[qb]);
-                        if (have_prev) {
-                            ok = issue_pv();
-                            if (!ok) break;
-                        }
-                        pg_ = g;
-                        pst = st;
-                        pseg = w.seg;
-                        pob = ob;
-                        pfirst = (jj == jb);
-                        plast = (jj == je - 1);
-                        have_prev = true;
                     }
-                    w.next(x, jb, je);
+                    if (gp < gs) {
+                        const int ob = cp.w.seg % C::kOBufs;
+                        bool ready = mbar_test(&ctrl->p_full[gp & 1], (uint32_t)((gp >> 1) & 1));
+                        if (ready && cp.first() && cp.w.seg >= C::kOBufs)
+                            ready = mbar_test(&ctrl->o_empty[ob], ((cp.w.seg / C::kOBufs) - 1) & 1);
+                        if (ready) {
+                            CPA_TRACE_EVENT(3, gp);
+                            tc_fence_after_sync();
+                            const int st = (int)(gp % p.n_stages);
+                            const uint32_t vb = sbase + p.off_kv + st * kStageBytes + 2 * kBN * 128;
+                            const bool first = cp.first();
+                            const int passes = (cp.jj == cp.x.n_tiles - 1) ? 2 : 1;
+                            for (int mt = 0; mt < NUM_MT; ++mt) {
+                                // P (bf16, two per column) sits in the first 32 columns of the
+                                // tile's S buffer, its residual in the next 32
+                                const uint32_t pa = tmem + C::s_col(mt, (int)(gp & 1));
+                                for (int pass = 0; pass < passes; ++pass) {
+#pragma unroll
+                                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                                        const uint64_t bd =
+                                            sdesc_sw128(vb + kk * 16 * 128, kBN * 128, 1024);
+                                        umma_bf16_ts(tmem + C::o_col(mt, ob), pa + pass * 32 + kk * 8,
+                                                     bd, idesc_o,
+                                                     (first && pass == 0 && kk == 0) ? 0u : 1u);
+                                    }
+                                }
+                            }
+                            umma_commit(&ctrl->p_empty[gp & 1]);
+                            umma_commit(&ctrl->kv_empty[st]);
+                            if (cp.last()) umma_commit(&ctrl->o_full[ob]);
+                            cp.advance(p);
+                            ++gp;
+                            progressed = true;
+                        }
+                    }
+                    if (progressed) {
+                        spins = 0;
+                    } else {
+                        // back off so the poll does not take issue slots from the
+                        // softmax warp that shares this SM sub-partition
+                        __nanosleep(20);
+                    }
+                    if (!progressed && (++spins & 63u) == 0) {
+                        // same time limit as every other wait of the kernel
+                        const uint64_t now = globaltimer_ns();
+                        if (spins == 64) t_idle = now;
+                        if (*abort_flag) {
+                            ok = false;
+                        } else if (now - t_idle > kWaitLimitNs) {
+                            atomicOr(p.status, CPA_DEV_TIMEOUT);
+                            *abort_flag = 1u;
+                            ok = false;
+                        }
+                        if (!ok) break;
+                    }
                 }
-                if (ok && have_prev) issue_pv();
                 umma_commit(&ctrl->mma_done);
                 mbar_wait(&ctrl->mma_done, 0, abort_flag, p.status);
             }
@@ -634,17 +726,37 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     tc_fence_after_sync();
                     uint32_t sr[64];
                     tmem_ld_x64(tmem + lane_addr + C::s_col(mt, (int)(g & 1)), sr);
+                    const bool dtile = jj >= x.n_prefix;
                     const int key0 = (x.tile_base + jj) * kBN;
-                    const bool whole = key0 >= lo && key0 + kBN <= hi;
-                    float tmax = neg_inf();
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const int key = key0 + c;
-                        const float s = __uint_as_float(sr[c]) * p.scale_log2;
-                        const float v = (whole || (key >= lo && key < hi)) ? s : neg_inf();
-                        sr[c] = __float_as_uint(v);
-                        tmax = fmaxf(tmax, v);
+                    // visible columns [lo_c, hi_c) of this tile for this row
+                    int lo_c, hi_c;
+                    if (dtile) {
+                        // drafts: row (branch k, draft s) sees drafts 0..s of branch k,
+                        // held in tile columns k*sb .. k*sb+s
+                        const bool casc = p.mode == MODE_CASCADE;
+                        lo_c = (casc ? it / p.S : 0) * p.sb;
+                        hi_c = it < x.ntok ? lo_c + (casc ? it % p.S : it) + 1 : lo_c;
+                    } else {
+                        lo_c = lo - key0;
+                        hi_c = hi - key0;
                     }
+                    // Raw-score maximum (the scale is positive, so it commutes with max);
+                    // masked keys become -inf.  Interior tiles skip the mask.
+                    float m4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
+                    if (lo_c <= 0 && hi_c >= kBN) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            const float v = (c >= lo_c && c < hi_c) ? __uint_as_float(sr[c])
+                                                                    : neg_inf();
+                            sr[c] = __float_as_uint(v);
+                            m4[c & 3] = fmaxf(m4[c & 3], v);
+                        }
+                    }
+                    const float tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
                     const bool need = (l > 0.f) && (tmax > m_used + kRescaleLog2);
                     if (__any_sync(0xffffffffu, need)) {
                         // O holds PV of tiles up to g-1 of this unit: wait for it, then rescale
@@ -669,34 +781,49 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     }
                     if (m_used == neg_inf()) m_used = tmax;
                     const float mref = (m_used == neg_inf()) ? 0.f : m_used;
-                    float sum = 0.f;
+                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
                     uint32_t pk[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        const float a = ex2(__uint_as_float(sr[2 * c]) - mref);
-                        const float b = ex2(__uint_as_float(sr[2 * c + 1]) - mref);
-                        sum += a + b;
+                        const float a = ex2(fmaf(__uint_as_float(sr[2 * c]), p.scale_log2, -mref));
+                        const float b =
+                            ex2(fmaf(__uint_as_float(sr[2 * c + 1]), p.scale_log2, -mref));
+                        s4[c & 3] += a + b;
                         pk[c] = pack_bf16x2(a, b);
                     }
+                    const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
                     l += sum;
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(5, g);
-                    // the P buffer this tile writes must no longer be read by an earlier PV
-                    if (C::kPBufs == 2) {
-                        if (g >= 2)
-                            ok = mbar_wait_warp(&ctrl->p_empty[g & 1], (uint32_t)(((g - 2) >> 1) & 1),
-                                           abort_flag, p.status);
-                    } else if (g >= 1) {
-                        ok = mbar_wait_warp(&ctrl->p_empty[(g - 1) & 1],
-                                       (uint32_t)(((g - 1) >> 1) & 1), abort_flag, p.status);
-                    }
-                    if (!ok) break;
-                    uint8_t* prow = smem + p.off_p + (mt * C::kPBufs + (int)(g % C::kPBufs)) * kPBytes +
-                                    r * 128;
+                    // P over the S columns of this tile (the MMA that produced S is done
+                    // and every earlier MMA too, so no PV still reads these columns)
+                    const uint32_t s_addr = tmem + lane_addr + C::s_col(mt, (int)(g & 1));
+                    tmem_st_x32(s_addr, pk);
+                    if (jj == x.n_tiles - 1) {
+                        // the unit's last tile: also store what the bf16 rounding of P
+                        // dropped (itself in bf16), for the second PV pass
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
-                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                    if (mt == 0 && key0 + kBN > x.valid_end) {
+                        for (int c = 0; c < 32; ++c) {
+                            const float a = ex2(fmaf(__uint_as_float(sr[2 * c]), p.scale_log2, -mref));
+                            const float b =
+                                ex2(fmaf(__uint_as_float(sr[2 * c + 1]), p.scale_log2, -mref));
+                            pk[c] = pack_bf16x2(a - __uint_as_float(pk[c] << 16),
+                                                b - __uint_as_float(pk[c] & 0xFFFF0000u));
+                        }
+                        tmem_st_x32(s_addr + 32, pk);
+                    }
+                    if (mt == 0 && dtile) {
+                        // rows of the draft tile that hold no draft (slots past S of a
+                        // branch's page, blocks past the last branch): zero their V so
+                        // that P = 0 there contributes exactly nothing
+                        const int st = (int)(g % p.n_stages);
+                        uint8_t* vb = smem + p.off_kv + st * kStageBytes + 2 * kBN * 128;
+                        for (int i = r; i < 2 * kBN * 8; i += 128) {
+                            const int half = i / (kBN * 8), row = (i / 8) % kBN;
+                            if (row >= p.nbr * p.sb || (row % p.sb) >= p.S)
+                                *reinterpret_cast<uint4*>(vb + half * kBN * 128 + row * 128 +
+                                                          (i % 8) * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                    } else if (mt == 0 && key0 + kBN > x.valid_end) {
                         // V rows past the sequence end hold whatever the page had (or stale
                         // data): zero them so that P = 0 there contributes exactly nothing.
                         const int first = max(0, x.valid_end - key0);
@@ -709,7 +836,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                 make_uint4(0, 0, 0, 0);
                         }
                     }
-                    fence_proxy_async_smem();
+                    fence_proxy_async_smem();  // V rows zeroed above are read by the MMA
                     tc_fence_before_sync();
                     mbar_arrive(&ctrl->p_full[g & 1]);
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(6, g);
@@ -726,15 +853,15 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             }
         } else if (warp >= C::kEpiWarp0) {
             // ============================== epilogue
+            // O / l for each row of a finished unit.  A unit split across CTAs is
+            // written as a partial (o, lse); the CTA that completes it last merges
+            // the partials in CTA order by the log-sum-exp identity.
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
             const int et = r;  // 0..127 within the epilogue warpgroup
             const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-            const bool verify_out = p.mode == MODE_CASCADE || p.mode == MODE_NAIVE;
             const bool fp32_out = p.mode == MODE_PASS_A || p.mode == MODE_PREFILL_RECT ||
                                   p.mode == MODE_PREFILL_TRI;
-            uint8_t* dk_s = smem + p.off_draft;
-            uint8_t* dv_s = dk_s + kMaxDraftKeys * 256;
             Walker w;
             w.init(ctrl);
             bool ok = true;
@@ -752,183 +879,88 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 if (et == 0) CPA_TRACE_EVENT(7, w.seg);
                 tc_fence_after_sync();
 
-                // stage this unit's draft K/V rows (verify) in shared memory
-                auto load_draft = [&]() {
-                    const int nk = p.draft_keys;
-                    for (int i = et; i < nk * 32; i += 128) {
-                        const int kx = i >> 5, part = i & 31;  // 16 chunks of K then 16 of V
-                        const int br = x.branch0 + kx / p.S, j = kx % p.S;
-                        const int pg = __ldg(p.dtab + (size_t)(x.b * p.topk + br) * p.dtab_stride +
-                                             j / p.P);
-                        uint4 v = make_uint4(0, 0, 0, 0);
-                        if (pg >= 0 && pg < p.num_pages) {
-                            const size_t off =
-                                (((size_t)pg * p.P + (j % p.P)) * p.H_kv + x.h) * 128 +
-                                (part & 15) * 8;
-                            const __nv_bfloat16* src = (part < 16 ? p.k_pages : p.v_pages) + off;
-                            v = __ldg(reinterpret_cast<const uint4*>(src));
-                        } else if (part == 0) {
-                            atomicOr(p.status, CPA_DEV_BAD_PAGE);
-                        }
-                        uint8_t* dst = (part < 16 ? dk_s : dv_s) + kx * 256 + (part & 15) * 16;
-                        *reinterpret_cast<uint4*>(dst) = v;
-                    }
-                };
-
-                // write one row's result; oa(c, f[8]) supplies o_A / sum for chunk c
-                auto finish_row = [&](int R, float lse2a, auto&& oa) {
+                // Write one row; oa(blk, f) supplies columns blk*32..+31 of its output.
+                auto finish_row = [&](int R, float lse2, auto&& oa) {
                     const int it = R / G, gq = R % G;
                     const bool valid = it < x.ntok;
                     const size_t orow = (size_t)(x.t0 + (valid ? it : 0)) * p.H_q + x.h * G + gq;
-                    if (!verify_out) {
 #pragma unroll 1
-                        for (int c = 0; c < 16; ++c) {
-                            float f[8];
-                            oa(c, f);
-                            if (valid) {
-                                if (fp32_out) {
-                                    float4* dst = reinterpret_cast<float4*>(
-                                        static_cast<float*>(p.o) + orow * 128 + c * 8);
-                                    dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-                                    dst[1] = make_float4(f[4], f[5], f[6], f[7]);
-                                } else {
-                                    *reinterpret_cast<uint4*>(
-                                        static_cast<__nv_bfloat16*>(p.o) + orow * 128 + c * 8) =
-                                        make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                                   pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-                                }
-                            }
-                        }
-                        if (valid) p.lse[orow] = lse2a == neg_inf() ? neg_inf() : lse2a * kLn2;
-                        return;
-                    }
-                    // own-branch drafts 0..s (Pass B) for this row, then the LSE merge
-                    const int sidx = valid ? it % p.S : 0;
-                    const int kb = (valid && p.mode == MODE_CASCADE) ? (it / p.S) * p.S : 0;
-                    const __nv_bfloat16* qrow = p.q + orow * 128;
-                    float sc[kMaxDraft];
-#pragma unroll
-                    for (int j = 0; j < kMaxDraft; ++j) sc[j] = 0.f;
-#pragma unroll 1
-                    for (int c = 0; c < 16; ++c) {
-                        float qf[8];
-                        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(qrow + c * 8)), qf);
-#pragma unroll
-                        for (int j = 0; j < kMaxDraft; ++j) {
-                            if (j <= sidx) {
-                                float kf[8];
-                                bf16x8_to_f32(*reinterpret_cast<const uint4*>(
-                                                  dk_s + (kb + j) * 256 + c * 16),
-                                              kf);
-                                float acc = sc[j];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) acc = fmaf(qf[e], kf[e], acc);
-                                sc[j] = acc;
-                            }
-                        }
-                    }
-                    float mb = neg_inf();
-#pragma unroll
-                    for (int j = 0; j < kMaxDraft; ++j) {
-                        sc[j] *= p.scale_log2;
-                        if (j <= sidx) mb = fmaxf(mb, sc[j]);
-                    }
-                    float lb = 0.f;
-#pragma unroll
-                    for (int j = 0; j < kMaxDraft; ++j) {
-                        sc[j] = (j <= sidx) ? ex2(sc[j] - mb) : 0.f;
-                        lb += sc[j];
-                    }
-                    const float lse2b = mb + lg2(lb);
-                    const float mx = fmaxf(lse2a, lse2b);
-                    const float wa = ex2(lse2a - mx), wb = ex2(lse2b - mx);
-                    const float tot = wa + wb;
-                    const float ca = wa / tot, cb = wb / (tot * lb);
-                    const float lse2 = mx + lg2(tot);
-#pragma unroll 1
-                    for (int c = 0; c < 16; ++c) {
-                        float f[8];
+                    for (int blk = 0; blk < 4; ++blk) {
+                        float f[32];
                         __syncwarp();
-                        oa(c, f);
+                        oa(blk, f);
+                        if (!valid) continue;
+                        if (fp32_out) {
+                            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) +
+                                                                    orow * 128 + blk * 32);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] *= ca;
+                            for (int e = 0; e < 8; ++e)
+                                dst[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2],
+                                                     f[4 * e + 3]);
+                        } else {
+                            uint4* dst = reinterpret_cast<uint4*>(
+                                static_cast<__nv_bfloat16*>(p.o) + orow * 128 + blk * 32);
 #pragma unroll
-                        for (int j = 0; j < kMaxDraft; ++j) {
-                            if (j <= sidx) {
-                                float vf[8];
-                                bf16x8_to_f32(*reinterpret_cast<const uint4*>(
-                                                  dv_s + (kb + j) * 256 + c * 16),
-                                              vf);
-                                const float wj = cb * sc[j];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) f[e] = fmaf(wj, vf[e], f[e]);
-                            }
+                            for (int e = 0; e < 4; ++e)
+                                dst[e] = make_uint4(pack_bf16x2(f[8 * e], f[8 * e + 1]),
+                                                    pack_bf16x2(f[8 * e + 2], f[8 * e + 3]),
+                                                    pack_bf16x2(f[8 * e + 4], f[8 * e + 5]),
+                                                    pack_bf16x2(f[8 * e + 6], f[8 * e + 7]));
                         }
-                        if (valid)
-                            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
-                                                      orow * 128 + c * 8) =
-                                make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                           pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
                     }
-                    if (valid) p.lse[orow] = lse2 * kLn2;
+                    if (valid) p.lse[orow] = lse2 == neg_inf() ? neg_inf() : lse2 * kLn2;
                 };
 
                 if (!split) {
-                    if (verify_out) {
-                        load_draft();
-                        named_bar_sync(1, 128);
-                    }
                     for (int mt = 0; mt < NUM_MT; ++mt) {
                         const int R = mt * 128 + r;
                         const float2 st = stats[ob * 256 + R];
-                        const float lse2a = st.y > 0.f ? st.x + lg2(st.y) : neg_inf();
+                        const float lse2 = st.y > 0.f ? st.x + lg2(st.y) : neg_inf();
                         const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
                         const uint32_t oaddr = tmem + lane_addr + C::o_col(mt, ob);
-                        finish_row(R, lse2a, [&](int c, float (&f)[8]) {
-                            uint32_t v[8];
-                            tmem_ld_x8(oaddr + c * 8, v);
+                        finish_row(R, lse2, [&](int blk, float (&f)[32]) {
+                            uint32_t v[32];
+                            tmem_ld_x32(oaddr + blk * 32, v);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[e]) * inv;
+                            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * inv;
                         });
                     }
                     tc_fence_before_sync();
                     mbar_arrive(&ctrl->o_empty[ob]);
-                    if (verify_out) named_bar_sync(1, 128);  // draft buffer reuse
                 } else {
                     const int slot = split_slot(total, n_ctas, blockIdx.x, w.ustart);
                     for (int mt = 0; mt < NUM_MT; ++mt) {
                         const int R = mt * 128 + r;
                         const float2 st = stats[ob * 256 + R];
-                        const float lse2a = st.y > 0.f ? st.x + lg2(st.y) : neg_inf();
+                        const float lse2 = st.y > 0.f ? st.x + lg2(st.y) : neg_inf();
                         const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
                         const uint32_t oaddr = tmem + lane_addr + C::o_col(mt, ob);
                         const bool valid = R / G < x.ntok;
                         float* po = p.part_o + ((size_t)slot * kMaxUnitRows + R) * 128;
 #pragma unroll 1
-                        for (int c = 0; c < 16; ++c) {
-                            uint32_t v[8];
-                            tmem_ld_x8(oaddr + c * 8, v);
+                        for (int blk = 0; blk < 4; ++blk) {
+                            uint32_t v[32];
+                            __syncwarp();
+                            tmem_ld_x32(oaddr + blk * 32, v);
                             if (valid) {
-                                float4* d4 = reinterpret_cast<float4*>(po + c * 8);
-                                d4[0] = make_float4(__uint_as_float(v[0]) * inv,
-                                                    __uint_as_float(v[1]) * inv,
-                                                    __uint_as_float(v[2]) * inv,
-                                                    __uint_as_float(v[3]) * inv);
-                                d4[1] = make_float4(__uint_as_float(v[4]) * inv,
-                                                    __uint_as_float(v[5]) * inv,
-                                                    __uint_as_float(v[6]) * inv,
-                                                    __uint_as_float(v[7]) * inv);
+                                float4* d4 = reinterpret_cast<float4*>(po + blk * 32);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    d4[e] = make_float4(__uint_as_float(v[4 * e]) * inv,
+                                                        __uint_as_float(v[4 * e + 1]) * inv,
+                                                        __uint_as_float(v[4 * e + 2]) * inv,
+                                                        __uint_as_float(v[4 * e + 3]) * inv);
                             }
                         }
-                        if (valid) p.part_lse[(size_t)slot * kMaxUnitRows + R] = lse2a;
+                        if (valid) p.part_lse[(size_t)slot * kMaxUnitRows + R] = lse2;
                     }
                     tc_fence_before_sync();
                     mbar_arrive(&ctrl->o_empty[ob]);
                     __threadfence();
                     named_bar_sync(1, 128);
+                    const int c_first = split_owner(total, n_ctas, w.ustart);
+                    const int c_last = split_owner(total, n_ctas, w.ustart + x.n_tiles - 1);
                     if (et == 0) {
-                        const int c_first = split_owner(total, n_ctas, w.ustart);
-                        const int c_last = split_owner(total, n_ctas, w.ustart + x.n_tiles - 1);
                         const unsigned old = atomicAdd(p.counters + w.u, 1u);
                         ctrl->flag = (old == (unsigned)(c_last - c_first)) ? 1 : 0;
                     }
@@ -936,58 +968,45 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     const bool last = *reinterpret_cast<volatile int*>(&ctrl->flag) != 0;
                     if (last) {
                         __threadfence();
-                        if (verify_out) {
-                            load_draft();
-                            named_bar_sync(1, 128);
-                        }
-                        const int c_first = split_owner(total, n_ctas, w.ustart);
-                        const int c_last = split_owner(total, n_ctas, w.ustart + x.n_tiles - 1);
+                        const int np = c_last - c_first + 1;
                         for (int mt = 0; mt < NUM_MT; ++mt) {
                             const int R = mt * 128 + r;
                             const bool valid = R / G < x.ntok;
+                            auto slot_of = [&](int c) -> size_t {
+                                return (size_t)split_slot(total, n_ctas, c_first + c, w.ustart) *
+                                           kMaxUnitRows + R;
+                            };
                             float mx = neg_inf();
                             if (valid)
-                                for (int c = c_first; c <= c_last; ++c)
-                                    mx = fmaxf(mx, __ldcg(p.part_lse +
-                                                          (size_t)split_slot(total, n_ctas, c,
-                                                                             w.ustart) *
-                                                              kMaxUnitRows +
-                                                          R));
+                                for (int c = 0; c < np; ++c)
+                                    mx = fmaxf(mx, __ldcg(p.part_lse + slot_of(c)));
                             float den = 0.f;
                             if (valid && mx != neg_inf())
-                                for (int c = c_first; c <= c_last; ++c)
-                                    den += ex2(__ldcg(p.part_lse +
-                                                      (size_t)split_slot(total, n_ctas, c,
-                                                                         w.ustart) *
-                                                          kMaxUnitRows +
-                                                      R) -
-                                               mx);
-                            const float lse2a = (den > 0.f) ? mx + lg2(den) : neg_inf();
-                            finish_row(R, lse2a, [&](int ch, float (&f)[8]) {
+                                for (int c = 0; c < np; ++c)
+                                    den += ex2(__ldcg(p.part_lse + slot_of(c)) - mx);
+                            const float lse2 = (den > 0.f) ? mx + lg2(den) : neg_inf();
+                            finish_row(R, lse2, [&](int blk, float (&f)[32]) {
 #pragma unroll
-                                for (int e = 0; e < 8; ++e) f[e] = 0.f;
+                                for (int e = 0; e < 32; ++e) f[e] = 0.f;
                                 if (!valid || den == 0.f) return;
-                                for (int c = c_first; c <= c_last; ++c) {
-                                    const size_t sl =
-                                        (size_t)split_slot(total, n_ctas, c, w.ustart) *
-                                            kMaxUnitRows +
-                                        R;
-                                    const float wc = ex2(__ldcg(p.part_lse + sl) - lse2a);
+                                for (int c = 0; c < np; ++c) {
+                                    const size_t sl = slot_of(c);
+                                    const float wc = ex2(__ldcg(p.part_lse + sl) - lse2);
                                     const float4* s4 =
-                                        reinterpret_cast<const float4*>(p.part_o + sl * 128 + ch * 8);
-                                    const float4 a = __ldcg(s4), b = __ldcg(s4 + 1);
-                                    f[0] = fmaf(wc, a.x, f[0]);
-                                    f[1] = fmaf(wc, a.y, f[1]);
-                                    f[2] = fmaf(wc, a.z, f[2]);
-                                    f[3] = fmaf(wc, a.w, f[3]);
-                                    f[4] = fmaf(wc, b.x, f[4]);
-                                    f[5] = fmaf(wc, b.y, f[5]);
-                                    f[6] = fmaf(wc, b.z, f[6]);
-                                    f[7] = fmaf(wc, b.w, f[7]);
+                                        reinterpret_cast<const float4*>(p.part_o + sl * 128 + blk * 32);
+                                    float4 v4[8];
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) v4[e] = __ldcg(s4 + e);
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        f[4 * e] = fmaf(wc, v4[e].x, f[4 * e]);
+                                        f[4 * e + 1] = fmaf(wc, v4[e].y, f[4 * e + 1]);
+                                        f[4 * e + 2] = fmaf(wc, v4[e].z, f[4 * e + 2]);
+                                        f[4 * e + 3] = fmaf(wc, v4[e].w, f[4 * e + 3]);
+                                    }
                                 }
                             });
                         }
-                        if (verify_out) named_bar_sync(1, 128);
                     }
                 }
                 if (et == 0) CPA_TRACE_EVENT(8, w.seg);

@@ -15,10 +15,8 @@ namespace cpa {
 
 // Keys per pipeline tile (one TMA stage, one N=64 QK^T MMA).
 constexpr int kBN = 64;
-// Draft tokens per branch the fused epilogue can hold in registers.
+// Draft tokens per branch of a verify unit (one draft tile holds every branch).
 constexpr int kMaxDraft = 16;
-// Draft keys per unit the epilogue's shared-memory buffer can hold.
-constexpr int kMaxDraftKeys = 32;
 // Rows of the partial-result slots (two 128-row M tiles).
 constexpr int kMaxUnitRows = 256;
 

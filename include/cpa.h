@@ -114,11 +114,12 @@ size_t cpa_cascade_verify_workspace_size(int B, int topk, int S, int H_q, int H_
  *   prefix_lens        int32 [B] on the device: L_b >= 0 ("cache_seqlens").
  *   max_prefix_len     host-side upper bound of every L_b; prefix_pt_stride
  *                      must be >= ceil(max_prefix_len / page_size).
- *   sm_scale           softmax scale, normally 1/sqrt(head_dim).
+ *   sm_scale           softmax scale (> 0), normally 1/sqrt(head_dim).
  *   o                  bf16 [B*topk*S, H_q, head_dim] output.
  *   lse                fp32 [B*topk*S, H_q] output (natural log).
- * Supported: head_dim 128; page_size in {8,16,32,64,128,256}; 1 <= S <= 16;
- * topk*S <= 32; topk*S*(H_q/H_kv) <= 256.
+ * Supported: head_dim 128; page_size in {8,16,32,64,128,256}; 1 <= S <= 16
+ * and S <= page_size (a branch's drafts share its first draft page);
+ * topk <= 8 when S <= 8, topk <= 4 when S > 8; topk*S*(H_q/H_kv) <= 256.
  */
 cpa_status cpa_cascade_verify(const void* q, const void* k_pages, const void* v_pages,
                               const int32_t* prefix_page_table, int prefix_pt_stride,
@@ -133,8 +134,8 @@ cpa_status cpa_cascade_verify(const void* q, const void* k_pages, const void* v_
  * as cpa_cascade_verify, but every branch (b, k) is run as its own request
  * over its L_b + S logical keys (prefix pages, then its own draft pages), so
  * each prefix is read topk times: B*topk*(L+S) KV tokens in total (cascade
- * page, "Naive Expand").  Supported: S*(H_q/H_kv) <= 256, other limits as
- * cpa_cascade_verify.  Workspace: cpa_cascade_verify_workspace_size.
+ * page, "Naive Expand").  Supported: S*(H_q/H_kv) <= 256, S <= 16,
+ * S <= page_size.  Workspace: cpa_cascade_verify_workspace_size.
  */
 cpa_status cpa_naive_expand_verify(const void* q, const void* k_pages, const void* v_pages,
                                    const int32_t* prefix_page_table, int prefix_pt_stride,
