@@ -93,9 +93,10 @@ struct Geometry {
     int smem_bytes;
 };
 
-// Shared-memory plan: control block and row statistics, Q buffers, then the
-// K/V stage ring.  As many stages as fit (up to 6), Q double-buffered when a
-// unit has a single M tile.
+// Shared-memory plan: control block, row statistics and exchange buffers,
+// then (units of two M tiles only) the Q tile, then the K/V stage ring with
+// as many 64 KB stages as fit (up to 4).  Units of one M tile keep Q in
+// tensor memory, double-buffered.
 bool plan_geometry(int G, int TS, Geometry& g) {
     const int rows = TS * G;
     if (rows <= 0 || rows > kMaxUnitRows) return false;
@@ -106,14 +107,14 @@ bool plan_geometry(int G, int TS, Geometry& g) {
     if (rows_mt > 128) return false;
     g.Rq = (rows_mt + 7) / 8 * 8;
     const size_t qmt = (size_t)2 * g.Rq * 128;
-    const int qb = g.num_mt == 1 ? 2 : 1;
+    g.n_qbufs = g.num_mt == 1 ? 2 : 1;
     const size_t off_q = kOffData;
-    const size_t off_kv = align_up(off_q + (size_t)qb * g.num_mt * qmt, 1024);
-    for (int st = 6; st >= 2; --st) {
+    const size_t q_bytes = g.num_mt == 1 ? 0 : (size_t)g.num_mt * qmt;
+    const size_t off_kv = align_up(off_q + q_bytes, 1024);
+    for (int st = 4; st >= 2; --st) {
         const size_t total = off_kv + (size_t)st * kStageBytes + 1024;
         if (total <= (size_t)kMaxSmemOptin) {
             g.n_stages = st;
-            g.n_qbufs = qb;
             g.off_q = (uint32_t)off_q;
             g.off_kv = (uint32_t)off_kv;
             g.smem_bytes = (int)total;

@@ -17,26 +17,28 @@
 //                                the same prefix read again for every k;
 //              prefill           one KV head and 128/G suffix tokens.
 //
-// Warp roles (warp index w):
+// Warp roles (warp index w, 16 warps):
 //   w = 0      producer: walks the block table (page ids prefetched 32 boxes
 //              ahead by the whole warp) and issues TMA loads of 128-B
-//              swizzled K/V boxes into a multi-stage ring, and of Q per unit;
-//   w = 1      MMA issuer: S = Q K^T (M=128, N=64, K=128) into TMEM, then
-//              O += P V (M=128, N=128, K=64) into TMEM;
-//   w = 4..    softmax, one warpgroup per 128-row M tile: reads its S row
-//              from TMEM, masks, exponentiates (base 2), writes bf16 P back
-//              over the S columns it came from (the PV MMA reads P from
-//              TMEM), and rescales O in TMEM only when the running max grew
-//              by more than 2^8.  On a unit's last tile (its drafts, or the
-//              causal diagonal) it also writes the bf16 residual of P, and PV
-//              runs twice, so rows that see few keys keep P to ~16 bits;
-//   last 4     epilogue: O / l, the merge of units split across CTAs, store.
+//              swizzled K/V boxes (one copy per lane) into a ring of 128-key
+//              stages; for units of two M tiles it also loads Q by TMA;
+//   w = 1      MMA issuer: S = Q K^T (M=128, N=128, K=128) into TMEM, then
+//              O += P V (M=128, N=128, K=128) into TMEM.  With one M tile Q
+//              sits in TMEM and both MMAs read their A operand from there;
+//   w = 4..11  softmax: two warpgroups.  With one M tile they split each
+//              tile's 128 columns and swap per-row maxima every tile; with
+//              two M tiles each owns one.  A thread reads its S row from TMEM,
+//              masks, exponentiates (base 2) and writes bf16 P back over the
+//              S columns it came from, rescaling O only when the running max
+//              grew by more than 2^8.  On a unit's last tile (its drafts, or
+//              the causal diagonal) it also writes the bf16 residual of P and
+//              PV runs twice, so rows that see few keys keep P to ~16 bits;
+//   w = 12..15 epilogue: O / l, the merge of units split across CTAs, store;
+//              with one M tile it also stages the next units' Q in TMEM.
 // Verify units end with one extra tile holding the unit's own draft tokens
 // (Pass B): branch k's drafts fill rows k*sb.. of that tile and the softmax
 // applies the causal-within-branch mask, so Pass B and its merge with Pass A
 // run inside the same online softmax on the tensor cores.
-// O is double-buffered in TMEM for one M tile, so the epilogue of one unit
-// overlaps the next unit's main loop.
 #pragma once
 #include <cstdint>
 
@@ -58,7 +60,7 @@ static __device__ unsigned long long* cpa_trace_buf = nullptr;
 #define CPA_TRACE_EVENT(ev, idx)                                                  \
     do {                                                                          \
         if (cpa_trace_buf && blockIdx.x < 4 && (idx) < 1024)                      \
-            cpa_trace_buf[(blockIdx.x * 16 + (ev)) * 1024 + (idx)] = clock64();   \
+            cpa_trace_buf[(blockIdx.x * 64 + (ev)) * 1024 + (idx)] = clock64();   \
     } while (0)
 #else
 #define CPA_TRACE_EVENT(ev, idx) \
@@ -206,10 +208,10 @@ __device__ __forceinline__ Unit get_unit(const AttnParams& p, int u) {
 
 // ------------------------------------------------------------------ shared control block
 struct Ctrl {
-    uint64_t kv_full[6], kv_empty[6];
+    uint64_t kv_full[4], kv_empty[4];
     uint64_t q_full[2], q_empty[2];
     uint64_t s_full[2], p_full[2], p_empty[2];
-    uint64_t o_full[2], o_empty[2], stats_full[2];
+    uint64_t o_full, o_empty, stats_full;
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t abort_flag;
@@ -225,21 +227,37 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= 1024, "control block");
 
-constexpr uint32_t kOffStats = 1024;  // float2 [2][256] of (max, sum) per row: 4 KB
-constexpr uint32_t kOffData = 5120;   // first 1024-aligned byte after the stats
-constexpr uint32_t kStageBytes = 4u * kBN * 128u;
+constexpr uint32_t kOffStats = 1024;  // float2 [256]: (max, sum) per row of a finished unit
+constexpr uint32_t kOffXchg = 3072;   // float [2][2][128]: per-half row maxima, by tile parity
+constexpr uint32_t kOffSum = 5120;    // float [128]: second half's row sums at a unit's end
+constexpr uint32_t kOffData = 6144;   // first 1024-aligned byte after the above
+constexpr uint32_t kStageBytes = 4u * kBN * 128u;  // K lo/hi, V lo/hi halves: 64 KB
 
+// Per-configuration layout.  NUM_MT = 1: units of up to 128 rows; Q lives in
+// TMEM (S = Q K^T reads its A operand from TMEM) and two softmax warpgroups
+// split each tile's 128 columns.  NUM_MT = 2: units of up to 256 rows in two
+// M tiles; Q lives in shared memory and each softmax warpgroup owns an M tile.
 template <int NUM_MT>
 struct Cfg {
-    static constexpr int kOBufs = NUM_MT == 1 ? 2 : 1;
-    static constexpr int kSmWarp0 = 4;
-    static constexpr int kEpiWarp0 = 4 + 4 * NUM_MT;
-    static constexpr int kThreads = 32 * (kEpiWarp0 + 4);
+    static constexpr bool kQInTmem = NUM_MT == 1;
+    static constexpr int kSplit = NUM_MT == 1 ? 2 : 1;  // softmax warpgroups per M tile
+    static constexpr int kSBufs = NUM_MT == 1 ? 2 : 1;  // S buffers per M tile
+    static constexpr int kSmWarp0 = 4;                   // 8 softmax warps: 4..11
+    static constexpr int kEpiWarp0 = 12;                 // 4 epilogue warps: 12..15
+    static constexpr int kThreads = 512;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t s_col(int mt, int sb) { return (uint32_t)(mt * 2 + sb) * kBN; }
-    static constexpr uint32_t o_col(int mt, int ob) {
-        return (uint32_t)(NUM_MT * 2 * kBN) + (uint32_t)(mt * kOBufs + ob) * 128u;
+    // TMEM columns.  Q (bf16, 2 per column): 64 per buffer; S: 128 per buffer
+    // (the P of each 64-key half overwrites the first 32 of that half's S
+    // columns, its residual the other 32); O: 128.
+    static constexpr uint32_t q_col(int qb) { return (uint32_t)qb * 64u; }
+    static constexpr uint32_t s_col(int mt, int sb) {
+        return (kQInTmem ? 128u : 0u) + (uint32_t)(mt * kSBufs + sb) * 128u;
     }
+    static constexpr uint32_t o_col(int mt) {
+        return (kQInTmem ? 128u : 0u) + (uint32_t)(NUM_MT * kSBufs) * 128u + (uint32_t)mt * 128u;
+    }
+    static_assert((kQInTmem ? 128 : 0) + NUM_MT * kSBufs * 128 + NUM_MT * 128 <= 512,
+                  "TMEM columns");
 };
 
 // Inclusive block-wide prefix sum of one int64 per thread; returns the
@@ -424,31 +442,33 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem);
     float2* stats = reinterpret_cast<float2*>(smem + kOffStats);
+    float* xchg = reinterpret_cast<float*>(smem + kOffXchg);
+    float* xsum = reinterpret_cast<float*>(smem + kOffSum);
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile uint32_t* abort_flag = &ctrl->abort_flag;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 6; ++i) {
+        for (int i = 0; i < 4; ++i) {
             mbar_init(&ctrl->kv_full[i], 1);
             mbar_init(&ctrl->kv_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&ctrl->q_full[i], 1);
+            mbar_init(&ctrl->q_full[i], C::kQInTmem ? 128 : 1);
             mbar_init(&ctrl->q_empty[i], 1);
             mbar_init(&ctrl->s_full[i], 1);
-            mbar_init(&ctrl->p_full[i], 128 * NUM_MT);
+            mbar_init(&ctrl->p_full[i], 256);
             mbar_init(&ctrl->p_empty[i], 1);
-            mbar_init(&ctrl->o_full[i], 1);
-            mbar_init(&ctrl->o_empty[i], 128);
-            mbar_init(&ctrl->stats_full[i], 128 * NUM_MT);
         }
+        mbar_init(&ctrl->o_full, 1);
+        mbar_init(&ctrl->o_empty, 128);
+        mbar_init(&ctrl->stats_full, 128 * NUM_MT);
         mbar_init(&ctrl->mma_done, 1);
         ctrl->abort_flag = 0;
         fence_barrier_init();
-        prefetch_tmap(&p.qmap);
         prefetch_tmap(&p.kmap);
         prefetch_tmap(&p.vmap);
+        if (!C::kQInTmem) prefetch_tmap(&p.qmap);
     }
     if (warp == 1) {
         tmem_alloc(&ctrl->tmem_base, C::kTmemCols);
@@ -458,6 +478,12 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     schedule(p, ctrl);
+#ifdef CPA_TRACE
+    if (threadIdx.x == 0 && cpa_trace_buf && blockIdx.x < 4) {
+        cpa_trace_buf[(blockIdx.x * 64 + 13) * 1024 + 1000] = clock64();
+        cpa_trace_buf[(blockIdx.x * 64 + 13) * 1024 + 1001] = globaltimer_ns();
+    }
+#endif
     const uint32_t tmem = ctrl->tmem_base;
     const int n_ctas = ctrl->n_ctas;
     const long long total = ctrl->total;
@@ -479,19 +505,21 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 const Unit x = get_unit(p, w.u);
                 int jb, je;
                 w.piece(x, jb, je);
-                const int qb = w.seg % p.n_qbufs;
-                if (w.seg >= p.n_qbufs)
-                    ok = mbar_wait_warp(&ctrl->q_empty[qb], ((w.seg / p.n_qbufs) - 1) & 1, abort_flag,
-                                   p.status);
-                if (!ok) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&ctrl->q_full[qb], q_tx);
-                    for (int mt = 0; mt < NUM_MT; ++mt) {
-                        uint8_t* dst = smem + p.off_q + (qb * NUM_MT + mt) * qmt_bytes;
-                        const int tok = x.t0 + mt * p.TSB;
-                        tma_load_3d(dst, &p.qmap, 0, x.h * G, tok, &ctrl->q_full[qb], pol_q);
-                        tma_load_3d(dst + p.Rq * 128, &p.qmap, 64, x.h * G, tok,
-                                    &ctrl->q_full[qb], pol_q);
+                if (!C::kQInTmem) {
+                    const int qb = w.seg % p.n_qbufs;
+                    if (w.seg >= p.n_qbufs)
+                        ok = mbar_wait_warp(&ctrl->q_empty[qb], ((w.seg / p.n_qbufs) - 1) & 1,
+                                            abort_flag, p.status);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&ctrl->q_full[qb], q_tx);
+                        for (int mt = 0; mt < NUM_MT; ++mt) {
+                            uint8_t* dst = smem + p.off_q + (qb * NUM_MT + mt) * qmt_bytes;
+                            const int tok = x.t0 + mt * p.TSB;
+                            tma_load_3d(dst, &p.qmap, 0, x.h * G, tok, &ctrl->q_full[qb], pol_q);
+                            tma_load_3d(dst + p.Rq * 128, &p.qmap, 64, x.h * G, tok,
+                                        &ctrl->q_full[qb], pol_q);
+                        }
                     }
                 }
                 // block-table window: lane l holds the page of box (wbase + l)
@@ -503,50 +531,54 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 int wbase = jb * NB;
                 int cur = load_page(wbase + lane);
                 int nxt = load_page(wbase + 32 + lane);
-                // first draft page of branch lane/4, if this piece ends with the draft tile
+                // first draft page of branch `lane`, if this piece ends with the draft tile
                 int dpage = -1;
-                if (p.has_draft && je == x.n_tiles && (lane >> 2) < p.nbr)
-                    dpage = __ldg(p.dtab + (size_t)(x.b * p.topk + x.branch0 + (lane >> 2)) *
-                                               p.dtab_stride);
+                if (p.has_draft && je == x.n_tiles && lane < p.nbr)
+                    dpage = __ldg(p.dtab + (size_t)(x.b * p.topk + x.branch0 + lane) * p.dtab_stride);
                 for (int jj = jb; jj < je; ++jj, ++g) {
                     const int st = (int)(g % p.n_stages);
                     if (g >= p.n_stages) {
-                        ok = mbar_wait_warp(&ctrl->kv_empty[st], (uint32_t)(((g / p.n_stages) - 1) & 1),
-                                       abort_flag, p.status);
+                        ok = mbar_wait_warp(&ctrl->kv_empty[st],
+                                            (uint32_t)(((g / p.n_stages) - 1) & 1), abort_flag,
+                                            p.status);
                         if (!ok) break;
                     }
+                    if (lane == 0) CPA_TRACE_EVENT(0, g);
+                    uint8_t* stage = smem + p.off_kv + st * kStageBytes;
                     if (jj >= x.n_prefix) {
                         // the unit's draft tile: branch k's drafts 0..S-1 sit in slots
-                        // 0..S-1 of its first draft page; lane 4k+part loads one
+                        // 0..S-1 of its first draft page; copy t = 4k + part loads one
                         // sb-row box (K lo/hi, V lo/hi) into rows k*sb.. of the tile
-                        if (lane == 0) CPA_TRACE_EVENT(0, g);
-                        const int k = lane >> 2, part = lane & 3;
-                        bool use = k < p.nbr;
+                        bool use = lane < p.nbr;
                         if (use && (dpage < 0 || dpage >= p.num_pages)) {
-                            if (part == 0) atomicOr(p.status, CPA_DEV_BAD_PAGE);
+                            atomicOr(p.status, CPA_DEV_BAD_PAGE);
                             use = false;
                         }
                         const uint32_t mask = __ballot_sync(0xffffffffu, use);
                         if (lane == 0)
                             mbar_arrive_expect_tx(&ctrl->kv_full[st],
-                                                  (uint32_t)__popc(mask) * p.sb * 128u);
+                                                  (uint32_t)__popc(mask) * 4u * p.sb * 128u);
                         __syncwarp();
-                        if (use) {
-                            uint8_t* dst = smem + p.off_kv + st * kStageBytes + part * (kBN * 128) +
-                                           k * p.sb * 128;
-                            tma_load_3d(dst, part < 2 ? &p.kdmap : &p.vdmap, (part & 1) * 64, x.h,
-                                        dpage * p.P, &ctrl->kv_full[st], pol_kv);
+                        // every lane runs the same iterations (the shuffle needs the whole
+                        // warp); only the copy itself is predicated
+                        for (int t0 = 0; t0 < 4 * p.nbr; t0 += 32) {
+                            const int t = t0 + lane;
+                            const int k = (t < 4 * p.nbr ? t : 0) >> 2, part = t & 3;
+                            const int pg = __shfl_sync(0xffffffffu, dpage, k & 31);
+                            if (t < 4 * p.nbr && (mask >> k & 1u))
+                                tma_load_3d(stage + part * (kBN * 128) + k * p.sb * 128,
+                                            part < 2 ? &p.kdmap : &p.vdmap, (part & 1) * 64, x.h,
+                                            pg * p.P, &ctrl->kv_full[st], pol_kv);
                         }
                         continue;
                     }
-                    if (lane == 0) CPA_TRACE_EVENT(0, g);
                     const int box0 = jj * NB;
                     if (box0 >= wbase + 32) {
                         cur = nxt;
                         wbase += 32;
                         nxt = load_page(wbase + 32 + lane);
                     }
-                    const int my_box = box0 + (lane & (NB - 1));
+                    const int my_box = box0 + (lane < NB ? lane : 0);
                     int pg = __shfl_sync(0xffffffffu, cur, (my_box - wbase) & 31);
                     const int pos = key_base + my_box * p.boxr;
                     bool use = lane < NB && pos < x.valid_end;
@@ -555,24 +587,24 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         use = false;
                     }
                     const uint32_t mask = __ballot_sync(0xffffffffu, use);
-                    if (lane == 0) {
-                        const uint32_t bytes = (uint32_t)__popc(mask) * 4u * p.boxr * 128u;
-                        mbar_arrive_expect_tx(&ctrl->kv_full[st], bytes);
-                    }
-                    // One TMA per lane: a thread issues TMA copies one after another,
-                    // so spreading the 4*NB boxes of a tile over 4*NB lanes keeps the
-                    // copy engine fed.  Lane l loads part l%4 (K lo/hi, V lo/hi
-                    // half) of box l/4.
-                    const int bi = lane >> 2, part = lane & 3;
-                    const int pgi = __shfl_sync(0xffffffffu, pg, bi & 31);
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(&ctrl->kv_full[st],
+                                              (uint32_t)__popc(mask) * 4u * p.boxr * 128u);
                     __syncwarp();
-                    if (bi < NB && (mask >> bi & 1u)) {
-                        const int posi = key_base + (box0 + bi) * p.boxr;
-                        const int row = pgi * p.P + (posi % p.P);
-                        uint8_t* dst = smem + p.off_kv + st * kStageBytes + part * (kBN * 128) +
-                                       bi * p.boxr * 128;
-                        tma_load_3d(dst, part < 2 ? &p.kmap : &p.vmap, (part & 1) * 64, x.h, row,
-                                    &ctrl->kv_full[st], pol_kv);
+                    // One TMA per lane: a thread issues its TMA copies one after another,
+                    // so the 4*NB boxes of a tile are spread over the lanes.  Copy t
+                    // loads part t%4 (K lo/hi, V lo/hi half) of box t/4.  Every lane runs
+                    // the same iterations (the shuffle needs the whole warp).
+                    for (int t0 = 0; t0 < 4 * NB; t0 += 32) {
+                        const int t = t0 + lane;
+                        const int bi = (t < 4 * NB ? t : 0) >> 2, part = t & 3;
+                        const int pgi = __shfl_sync(0xffffffffu, pg, bi & 31);
+                        if (t < 4 * NB && (mask >> bi & 1u)) {
+                            const int posi = key_base + (box0 + bi) * p.boxr;
+                            tma_load_3d(stage + part * (kBN * 128) + bi * p.boxr * 128,
+                                        part < 2 ? &p.kmap : &p.vmap, (part & 1) * 64, x.h,
+                                        pgi * p.P + (posi % p.P), &ctrl->kv_full[st], pol_kv);
+                        }
                     }
                 }
                 w.next(x, jb, je);
@@ -589,9 +621,8 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
         } else if (warp == 1) {
             // ============================== MMA issuer
             // Two cursors walk the same tile sequence: one issues S = Q K^T as soon
-            // as a tile's K/V and Q have landed, the other issues O += P V as soon
-            // as the softmax has written that tile's P.  Whichever is ready goes
-            // first, so a late K/V tile never holds back the PV that frees a stage.
+            // as a tile's K/V and Q are in place, the other O += P V as soon as the
+            // softmax has written that tile's P.  Whichever is ready goes first.
             if (lane == 0) {
                 const uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
                 const uint32_t idesc_o = idesc_bf16_f32(128, 128, true);
@@ -606,40 +637,49 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 bool ok = true;
                 while (gp < n_tiles) {
                     bool progressed = false;
-                    if (gs < n_tiles && gs <= gp + 1) {
+                    // S of tile gs overwrites the buffer that PV of tile gs - kSBufs reads
+                    if (gs < n_tiles && gs <= gp + C::kSBufs - 1) {
                         const int qb = cs.w.seg % p.n_qbufs;
                         const int st = (int)(gs % p.n_stages);
                         const bool q_ready =
                             !cs.first() || mbar_test(&ctrl->q_full[qb], (cs.w.seg / p.n_qbufs) & 1);
-                        if (q_ready && mbar_test(&ctrl->kv_full[st], (uint32_t)((gs / p.n_stages) & 1))) {
+                        if (q_ready &&
+                            mbar_test(&ctrl->kv_full[st], (uint32_t)((gs / p.n_stages) & 1))) {
                             CPA_TRACE_EVENT(2, gs);
                             tc_fence_after_sync();
-                            const int sb = (int)(gs & 1);
+                            const int sb = (int)(gs % C::kSBufs);
                             const uint32_t kb = sbase + p.off_kv + st * kStageBytes;
                             for (int mt = 0; mt < NUM_MT; ++mt) {
                                 const uint32_t qa = sbase + p.off_q + (qb * NUM_MT + mt) * qmt_bytes;
 #pragma unroll
                                 for (int kk = 0; kk < 8; ++kk) {
-                                    const uint64_t ad = sdesc_sw128(
-                                        qa + (kk >> 2) * p.Rq * 128 + (kk & 3) * 32, 16, 1024);
                                     const uint64_t bd = sdesc_sw128(
                                         kb + (kk >> 2) * kBN * 128 + (kk & 3) * 32, 16, 1024);
-                                    umma_bf16_ss(tmem + C::s_col(mt, sb), ad, bd, idesc_s,
-                                                 kk > 0 ? 1u : 0u);
+                                    if (C::kQInTmem) {
+                                        umma_bf16_ts(tmem + C::s_col(mt, sb),
+                                                     tmem + C::q_col(qb) + kk * 8, bd, idesc_s,
+                                                     kk > 0 ? 1u : 0u);
+                                    } else {
+                                        const uint64_t ad = sdesc_sw128(
+                                            qa + (kk >> 2) * p.Rq * 128 + (kk & 3) * 32, 16, 1024);
+                                        umma_bf16_ss(tmem + C::s_col(mt, sb), ad, bd, idesc_s,
+                                                     kk > 0 ? 1u : 0u);
+                                    }
                                 }
                             }
                             umma_commit(&ctrl->s_full[sb]);
                             if (cs.last()) umma_commit(&ctrl->q_empty[qb]);
+                            CPA_TRACE_EVENT(15, gs);
                             cs.advance(p);
                             ++gs;
                             progressed = true;
                         }
                     }
                     if (gp < gs) {
-                        const int ob = cp.w.seg % C::kOBufs;
-                        bool ready = mbar_test(&ctrl->p_full[gp & 1], (uint32_t)((gp >> 1) & 1));
-                        if (ready && cp.first() && cp.w.seg >= C::kOBufs)
-                            ready = mbar_test(&ctrl->o_empty[ob], ((cp.w.seg / C::kOBufs) - 1) & 1);
+                        bool ready = mbar_test(&ctrl->p_full[gp % C::kSBufs],
+                                               (uint32_t)((gp / C::kSBufs) & 1));
+                        if (ready && cp.first() && cp.w.seg >= 1)
+                            ready = mbar_test(&ctrl->o_empty, (uint32_t)((cp.w.seg - 1) & 1));
                         if (ready) {
                             CPA_TRACE_EVENT(3, gp);
                             tc_fence_after_sync();
@@ -648,23 +688,26 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                             const bool first = cp.first();
                             const int passes = (cp.jj == cp.x.n_tiles - 1) ? 2 : 1;
                             for (int mt = 0; mt < NUM_MT; ++mt) {
-                                // P (bf16, two per column) sits in the first 32 columns of the
-                                // tile's S buffer, its residual in the next 32
-                                const uint32_t pa = tmem + C::s_col(mt, (int)(gp & 1));
+                                // P of keys 64c..64c+63 (bf16, two per column) sits in the
+                                // first 32 of the 64 S columns those keys came from, its
+                                // residual in the other 32
+                                const uint32_t pa = tmem + C::s_col(mt, (int)(gp % C::kSBufs));
                                 for (int pass = 0; pass < passes; ++pass) {
 #pragma unroll
                                     for (int kk = 0; kk < kBN / 16; ++kk) {
                                         const uint64_t bd =
                                             sdesc_sw128(vb + kk * 16 * 128, kBN * 128, 1024);
-                                        umma_bf16_ts(tmem + C::o_col(mt, ob), pa + pass * 32 + kk * 8,
+                                        umma_bf16_ts(tmem + C::o_col(mt),
+                                                     pa + (kk >> 2) * 64 + pass * 32 + (kk & 3) * 8,
                                                      bd, idesc_o,
                                                      (first && pass == 0 && kk == 0) ? 0u : 1u);
                                     }
                                 }
                             }
-                            umma_commit(&ctrl->p_empty[gp & 1]);
+                            umma_commit(&ctrl->p_empty[gp % C::kSBufs]);
                             umma_commit(&ctrl->kv_empty[st]);
-                            if (cp.last()) umma_commit(&ctrl->o_full[ob]);
+                            if (cp.last()) umma_commit(&ctrl->o_full);
+                            CPA_TRACE_EVENT(14, gp);
                             cp.advance(p);
                             ++gp;
                             progressed = true;
@@ -673,9 +716,16 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     if (progressed) {
                         spins = 0;
                     } else {
-                        // back off so the poll does not take issue slots from the
-                        // softmax warp that shares this SM sub-partition
-                        __nanosleep(20);
+                        // Nothing ready: suspend on the barrier that gates the next PV
+                        // (it frees a K/V stage), or on the next K/V tile when no PV is
+                        // pending.  The thread wakes when the phase completes; the hint
+                        // bounds the wait so the other barrier is re-checked.
+                        if (gp < gs)
+                            mbar_try_wait_hint(&ctrl->p_full[gp % C::kSBufs],
+                                               (uint32_t)((gp / C::kSBufs) & 1), 200);
+                        else if (gs < n_tiles)
+                            mbar_try_wait_hint(&ctrl->kv_full[(int)(gs % p.n_stages)],
+                                               (uint32_t)((gs / p.n_stages) & 1), 200);
                     }
                     if (!progressed && (++spins & 63u) == 0) {
                         // same time limit as every other wait of the kernel
@@ -697,11 +747,19 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             __syncwarp();
         } else if (warp >= C::kSmWarp0 && warp < C::kEpiWarp0) {
             // ============================== softmax
-            const int mt = (warp - C::kSmWarp0) >> 2;
+            // NUM_MT = 1: warpgroup `half` handles columns [64*half, 64*half + 64) of
+            // every 128-key tile for all 128 rows; the two threads of a row swap
+            // their partial maxima each tile so both apply the same running max.
+            // NUM_MT = 2: warpgroup `mt` handles all 128 columns of its M tile.
+            const int wgi = (warp - C::kSmWarp0) >> 2;
+            const int mt = C::kSplit == 2 ? 0 : wgi;
+            const int half = C::kSplit == 2 ? wgi : 0;
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
             const int R = mt * 128 + r;
             const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+            const uint32_t o_addr = tmem + lane_addr + C::o_col(mt);
+            constexpr int kChunks = 2 / C::kSplit;  // 64-column chunks per thread
             Walker w;
             w.init(ctrl);
             long long g = 0;
@@ -710,22 +768,22 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 const Unit x = get_unit(p, w.u);
                 int jb, je;
                 w.piece(x, jb, je);
-                const int ob = w.seg % C::kOBufs;
                 const int it = R / G;
                 int lo = x.lo, hi;
                 if (is_verify(p.mode) || p.mode == MODE_PREFILL_RECT) hi = x.hi;
                 else hi = p.H_hit + x.p0 + it + 1;
-                if (it >= x.ntok) hi = lo;  // rows past the unit's tokens see nothing
+                // running max (log2 units, scaled) and this thread's part of the sum.
+                // Rows past the unit's tokens are computed over whole tiles like the
+                // others, so that a warp holding both kinds takes the unmasked path;
+                // their results stay in their own O rows and are never written.
                 float m_used = neg_inf(), l = 0.f;
-                const uint32_t o_addr = tmem + lane_addr + C::o_col(mt, ob);
+                const bool warp_inert = __all_sync(0xffffffffu, it >= x.ntok);
                 for (int jj = jb; jj < je; ++jj, ++g) {
-                    ok = mbar_wait_warp(&ctrl->s_full[g & 1], (uint32_t)((g >> 1) & 1), abort_flag,
-                                   p.status);
-                    if (!ok) break;
+                    const int sb = (int)(g % C::kSBufs);
+                    bool okl = mbar_wait_warp(&ctrl->s_full[sb], (uint32_t)((g / C::kSBufs) & 1),
+                                              abort_flag, p.status);
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(4, g);
-                    tc_fence_after_sync();
-                    uint32_t sr[64];
-                    tmem_ld_x64(tmem + lane_addr + C::s_col(mt, (int)(g & 1)), sr);
+                    if (lane == 0) CPA_TRACE_EVENT(20 + warp - C::kSmWarp0, g);
                     const bool dtile = jj >= x.n_prefix;
                     const int key0 = (x.tile_base + jj) * kBN;
                     // visible columns [lo_c, hi_c) of this tile for this row
@@ -740,128 +798,263 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         lo_c = lo - key0;
                         hi_c = hi - key0;
                     }
-                    // Raw-score maximum (the scale is positive, so it commutes with max);
-                    // masked keys become -inf.  Interior tiles skip the mask.
-                    float m4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
-                    if (lo_c <= 0 && hi_c >= kBN) {
+                    if (it >= x.ntok) {
+                        lo_c = 0;
+                        hi_c = kBN;
+                    }
+                    const uint32_t s_addr = tmem + lane_addr + C::s_col(mt, sb);
+                    if (okl) tc_fence_after_sync();
+                    // pass 1: this thread's raw maximum over its columns
+                    float tmax_raw = neg_inf();
+                    if (okl && !warp_inert) {
+#pragma unroll 1
+                        for (int ch = 0; ch < kChunks; ++ch) {
+                            const int c0 = (half + ch) * 64;
+                            uint32_t sr[64];
+                            tmem_ld_x64(s_addr + c0, sr);
+                            float m4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
+                            if (lo_c <= c0 && hi_c >= c0 + 64) {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
-                    } else {
+                                for (int c = 0; c < 64; ++c)
+                                    m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+                            } else {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) {
-                            const float v = (c >= lo_c && c < hi_c) ? __uint_as_float(sr[c])
-                                                                    : neg_inf();
-                            sr[c] = __float_as_uint(v);
-                            m4[c & 3] = fmaxf(m4[c & 3], v);
+                                for (int c = 0; c < 64; ++c)
+                                    if (c0 + c >= lo_c && c0 + c < hi_c)
+                                        m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+                            }
+                            tmax_raw = fmaxf(tmax_raw, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
                         }
                     }
-                    const float tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
-                    const bool need = (l > 0.f) && (tmax > m_used + kRescaleLog2);
-                    if (__any_sync(0xffffffffu, need)) {
-                        // O holds PV of tiles up to g-1 of this unit: wait for it, then rescale
-                        ok = mbar_wait_warp(&ctrl->p_empty[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1),
-                                       abort_flag, p.status);
-                        if (!ok) break;
-                        tc_fence_after_sync();
-                        const float f = need ? ex2(m_used - tmax) : 1.f;
+                    if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(13, g);
+                    if (lane == 0) CPA_TRACE_EVENT(28 + warp - C::kSmWarp0, g);
+                    if (C::kSplit == 2) {
+                        // swap partial maxima with the other half of the row; the barrier
+                        // also makes the timeout decision common to all 256 threads
+                        xchg[((int)(g & 1) * 2 + half) * 128 + r] = tmax_raw;
+                        okl = bar_and(2, 256, okl);
+                        tmax_raw = fmaxf(tmax_raw, xchg[((int)(g & 1) * 2 + (half ^ 1)) * 128 + r]);
+                    }
+                    if (!okl) {
+                        ok = false;
+                        break;
+                    }
+                    if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(1, g);
+                    if (lane == 0) CPA_TRACE_EVENT(36 + warp - C::kSmWarp0, g);
+                    if (!warp_inert) {
+                        const float tmax = tmax_raw * p.scale_log2;
+                        const bool need = (m_used != neg_inf()) && (tmax > m_used + kRescaleLog2);
+                        if (__any_sync(0xffffffffu, need)) {
+                            // O holds PV of tiles up to g-1 of this unit: wait for it, then
+                            // scale this thread's columns of O for rows whose max jumped
+                            const int pb = (int)((g - 1) % C::kSBufs);
+                            if (!mbar_wait_warp(&ctrl->p_empty[pb],
+                                                (uint32_t)(((g - 1) / C::kSBufs) & 1), abort_flag,
+                                                p.status)) {
+                                ok = false;  // the next barrier vote carries it to all threads
+                            } else {
+                                tc_fence_after_sync();
+                                const float f = need ? ex2(m_used - tmax) : 1.f;
+#pragma unroll 1
+                                for (int c4 = 0; c4 < 4 / C::kSplit; ++c4) {
+                                    const uint32_t oc = (uint32_t)(half * 64 + c4 * 32);
+                                    uint32_t ov[32];
+                                    tmem_ld_x32(o_addr + oc, ov);
 #pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4) {
-                            uint32_t ov[32];
-                            tmem_ld_x32(o_addr + c4 * 32, ov);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
-                            tmem_st_x32(o_addr + c4 * 32, ov);
+                                    for (int i = 0; i < 32; ++i)
+                                        ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+                                    tmem_st_x32(o_addr + oc, ov);
+                                }
+                                if (need) {
+                                    l *= f;
+                                    m_used = tmax;
+                                }
+                            }
                         }
-                        if (need) {
-                            l *= f;
-                            m_used = tmax;
+                        if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(17, g);
+                        if (m_used == neg_inf()) m_used = tmax;
+                        const float mref = (m_used == neg_inf()) ? 0.f : m_used;
+                        const bool resid = jj == x.n_tiles - 1;
+                        // pass 2: P = 2^(s*scale - mref) in bf16 over the S columns it came
+                        // from, inside the chunk's own 64 columns, so no chunk's P lands on
+                        // S another thread or chunk has yet to read (the MMA that produced
+                        // S is done, and so is every earlier MMA: no PV still reads them)
+#pragma unroll 1
+                        for (int ch = 0; ch < kChunks; ++ch) {
+                            const int c0 = (half + ch) * 64;
+                            const bool whole = lo_c <= c0 && hi_c >= c0 + 64;
+                            if (__all_sync(0xffffffffu, whole && !resid)) {
+                                // every column visible, no residual: two 32-column pieces,
+                                // each one's P stored over S columns already read
+                                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                                for (int sc = 0; sc < 2; ++sc) {
+                                    uint32_t sv[32], pk[16];
+                                    tmem_ld_x32(s_addr + (uint32_t)(c0 + 32 * sc), sv);
+#pragma unroll
+                                    for (int c = 0; c < 16; ++c) {
+                                        const float a =
+                                            ex2(fmaf(__uint_as_float(sv[2 * c]), p.scale_log2, -mref));
+                                        const float b = ex2(
+                                            fmaf(__uint_as_float(sv[2 * c + 1]), p.scale_log2, -mref));
+                                        s4[c & 3] += a + b;
+                                        pk[c] = pack_bf16x2(a, b);
+                                    }
+                                    tmem_st_x16_nowait(s_addr + (uint32_t)(c0 + 16 * sc), pk);
+                                }
+                                tmem_wait_st();
+                                l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                                continue;
+                            }
+                            uint32_t sr[64];
+                            tmem_ld_x64(s_addr + c0, sr);
+                            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                            uint32_t pk[32];
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) {
+                                const int ca = c0 + 2 * c;
+                                float xa = __uint_as_float(sr[2 * c]);
+                                float xb = __uint_as_float(sr[2 * c + 1]);
+                                if (!whole) {
+                                    if (ca < lo_c || ca >= hi_c) xa = neg_inf();
+                                    if (ca + 1 < lo_c || ca + 1 >= hi_c) xb = neg_inf();
+                                }
+                                const float a = ex2(fmaf(xa, p.scale_log2, -mref));
+                                const float b = ex2(fmaf(xb, p.scale_log2, -mref));
+                                s4[c & 3] += a + b;
+                                pk[c] = pack_bf16x2(a, b);
+                            }
+                            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                            if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(16, g);
+                            tmem_st_x32(s_addr + (uint32_t)c0, pk);
+                            if (resid) {
+                                // the unit's last tile: also store what the bf16 rounding
+                                // of P dropped (itself in bf16) for a second PV pass
+#pragma unroll
+                                for (int c = 0; c < 32; ++c) {
+                                    const int ca = c0 + 2 * c;
+                                    float xa = __uint_as_float(sr[2 * c]);
+                                    float xb = __uint_as_float(sr[2 * c + 1]);
+                                    if (!whole) {
+                                        if (ca < lo_c || ca >= hi_c) xa = neg_inf();
+                                        if (ca + 1 < lo_c || ca + 1 >= hi_c) xb = neg_inf();
+                                    }
+                                    const float a = ex2(fmaf(xa, p.scale_log2, -mref));
+                                    const float b = ex2(fmaf(xb, p.scale_log2, -mref));
+                                    pk[c] = pack_bf16x2(a - __uint_as_float(pk[c] << 16),
+                                                        b - __uint_as_float(pk[c] & 0xFFFF0000u));
+                                }
+                                tmem_st_x32(s_addr + (uint32_t)c0 + 32, pk);
+                            }
                         }
                     }
-                    if (m_used == neg_inf()) m_used = tmax;
-                    const float mref = (m_used == neg_inf()) ? 0.f : m_used;
-                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const float a = ex2(fmaf(__uint_as_float(sr[2 * c]), p.scale_log2, -mref));
-                        const float b =
-                            ex2(fmaf(__uint_as_float(sr[2 * c + 1]), p.scale_log2, -mref));
-                        s4[c & 3] += a + b;
-                        pk[c] = pack_bf16x2(a, b);
-                    }
-                    const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                    l += sum;
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(5, g);
-                    // P over the S columns of this tile (the MMA that produced S is done
-                    // and every earlier MMA too, so no PV still reads these columns)
-                    const uint32_t s_addr = tmem + lane_addr + C::s_col(mt, (int)(g & 1));
-                    tmem_st_x32(s_addr, pk);
-                    if (jj == x.n_tiles - 1) {
-                        // the unit's last tile: also store what the bf16 rounding of P
-                        // dropped (itself in bf16), for the second PV pass
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const float a = ex2(fmaf(__uint_as_float(sr[2 * c]), p.scale_log2, -mref));
-                            const float b =
-                                ex2(fmaf(__uint_as_float(sr[2 * c + 1]), p.scale_log2, -mref));
-                            pk[c] = pack_bf16x2(a - __uint_as_float(pk[c] << 16),
-                                                b - __uint_as_float(pk[c] & 0xFFFF0000u));
-                        }
-                        tmem_st_x32(s_addr + 32, pk);
-                    }
-                    if (mt == 0 && dtile) {
+                    if (lane == 0) CPA_TRACE_EVENT(44 + warp - C::kSmWarp0, g);
+                    bool zeroed = false;
+                    if (wgi == 0 && dtile) {
                         // rows of the draft tile that hold no draft (slots past S of a
                         // branch's page, blocks past the last branch): zero their V so
                         // that P = 0 there contributes exactly nothing
                         const int st = (int)(g % p.n_stages);
                         uint8_t* vb = smem + p.off_kv + st * kStageBytes + 2 * kBN * 128;
                         for (int i = r; i < 2 * kBN * 8; i += 128) {
-                            const int half = i / (kBN * 8), row = (i / 8) % kBN;
+                            const int hh = i / (kBN * 8), row = (i / 8) % kBN;
                             if (row >= p.nbr * p.sb || (row % p.sb) >= p.S)
-                                *reinterpret_cast<uint4*>(vb + half * kBN * 128 + row * 128 +
+                                *reinterpret_cast<uint4*>(vb + hh * kBN * 128 + row * 128 +
                                                           (i % 8) * 16) = make_uint4(0, 0, 0, 0);
                         }
-                    } else if (mt == 0 && key0 + kBN > x.valid_end) {
+                        zeroed = true;
+                    } else if (wgi == 0 && key0 + kBN > x.valid_end) {
                         // V rows past the sequence end hold whatever the page had (or stale
-                        // data): zero them so that P = 0 there contributes exactly nothing.
+                        // data): zero them so that P = 0 there contributes exactly nothing
                         const int first = max(0, x.valid_end - key0);
                         const int st = (int)(g % p.n_stages);
                         uint8_t* vb = smem + p.off_kv + st * kStageBytes + 2 * kBN * 128;
                         const int n16 = (kBN - first) * 8;  // 16-B chunks per half
                         for (int i = r; i < 2 * n16; i += 128) {
-                            const int half = i / n16, rem = i % n16;
-                            *reinterpret_cast<uint4*>(vb + half * kBN * 128 + first * 128 + rem * 16) =
+                            const int hh = i / n16, rem = i % n16;
+                            *reinterpret_cast<uint4*>(vb + hh * kBN * 128 + first * 128 + rem * 16) =
                                 make_uint4(0, 0, 0, 0);
                         }
+                        zeroed = true;
                     }
-                    fence_proxy_async_smem();  // V rows zeroed above are read by the MMA
+                    if (zeroed) fence_proxy_async_smem();  // the MMA reads those V rows
                     tc_fence_before_sync();
-                    mbar_arrive(&ctrl->p_full[g & 1]);
+                    mbar_arrive(&ctrl->p_full[sb]);
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(6, g);
+                    if (lane == 0 && wgi == 0) CPA_TRACE_EVENT(9 + quarter, g);
+                }
+                if (C::kSplit == 2) {
+                    // the second half hands its part of each row sum to the first
+                    if (half == 1) xsum[r] = l;
+                    ok = bar_and(3, 256, ok);
+                    if (half == 0) l += xsum[r];
                 }
                 if (!ok) break;
-                if (w.seg >= C::kOBufs) {
-                    ok = mbar_wait_warp(&ctrl->o_empty[ob], ((w.seg / C::kOBufs) - 1) & 1, abort_flag,
-                                   p.status);
-                    if (!ok) break;
+                if (half == 0) {
+                    if (w.seg >= 1) {
+                        ok = mbar_wait_warp(&ctrl->o_empty, (uint32_t)((w.seg - 1) & 1), abort_flag,
+                                            p.status);
+                    }
+                    if (ok) {
+                        stats[R] = make_float2(m_used, l);
+                        mbar_arrive(&ctrl->stats_full);
+                    }
                 }
-                stats[ob * 256 + R] = make_float2(m_used, l);
-                mbar_arrive(&ctrl->stats_full[ob]);
+                if (C::kSplit == 2) ok = bar_and(3, 256, ok);  // xsum and stats reuse
                 w.next(x, jb, je);
             }
         } else if (warp >= C::kEpiWarp0) {
             // ============================== epilogue
             // O / l for each row of a finished unit.  A unit split across CTAs is
             // written as a partial (o, lse); the CTA that completes it last merges
-            // the partials in CTA order by the log-sum-exp identity.
+            // the partials in CTA order by the log-sum-exp identity.  With one M
+            // tile, this warpgroup also loads each unit's Q rows into TMEM two
+            // units ahead of use.
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
             const int et = r;  // 0..127 within the epilogue warpgroup
             const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
             const bool fp32_out = p.mode == MODE_PASS_A || p.mode == MODE_PREFILL_RECT ||
                                   p.mode == MODE_PREFILL_TRI;
+            // Q of one unit into TMEM buffer qb: row r is query token r / G, head r % G
+            auto load_q = [&](const Unit& xu, int qb) {
+                const int it = r / G, gq = r % G;
+                uint32_t v[64];
+                if (it < xu.ntok) {
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        p.q + ((size_t)(xu.t0 + it) * p.H_q + xu.h * G + gq) * 128);
+                    uint4 u[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) u[c] = __ldg(src + c);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        v[4 * c] = u[c].x;
+                        v[4 * c + 1] = u[c].y;
+                        v[4 * c + 2] = u[c].z;
+                        v[4 * c + 3] = u[c].w;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) v[c] = 0u;
+                }
+                __syncwarp();
+                tmem_st_x64(tmem + lane_addr + C::q_col(qb), v);
+                tc_fence_before_sync();
+                mbar_arrive(&ctrl->q_full[qb]);
+            };
+            Walker wq;  // runs two units ahead of `w` to stage Q
+            wq.init(ctrl);
+            int q_loaded = 0;
+            if (C::kQInTmem) {
+                for (; q_loaded < 2 && wq.left > 0; ++q_loaded) {
+                    const Unit xq = get_unit(p, wq.u);
+                    int qjb, qje;
+                    wq.piece(xq, qjb, qje);
+                    load_q(xq, q_loaded);
+                    wq.next(xq, qjb, qje);
+                }
+            }
             Walker w;
             w.init(ctrl);
             bool ok = true;
@@ -870,10 +1063,9 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 int jb, je;
                 w.piece(x, jb, je);
                 const bool split = jb > 0 || je < x.n_tiles;
-                const int ob = w.seg % C::kOBufs;
-                const uint32_t ph = (uint32_t)((w.seg / C::kOBufs) & 1);
-                ok = mbar_wait(&ctrl->o_full[ob], ph, abort_flag, p.status) &&
-                     mbar_wait(&ctrl->stats_full[ob], ph, abort_flag, p.status);
+                const uint32_t ph = (uint32_t)(w.seg & 1);
+                ok = mbar_wait(&ctrl->o_full, ph, abort_flag, p.status) &&
+                     mbar_wait(&ctrl->stats_full, ph, abort_flag, p.status);
                 ok = bar_and(1, 128, ok);  // one decision for the whole epilogue warpgroup
                 if (!ok) break;
                 if (et == 0) CPA_TRACE_EVENT(7, w.seg);
@@ -914,10 +1106,10 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 if (!split) {
                     for (int mt = 0; mt < NUM_MT; ++mt) {
                         const int R = mt * 128 + r;
-                        const float2 st = stats[ob * 256 + R];
+                        const float2 st = stats[R];
                         const float lse2 = st.y > 0.f ? st.x + lg2(st.y) : neg_inf();
                         const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
-                        const uint32_t oaddr = tmem + lane_addr + C::o_col(mt, ob);
+                        const uint32_t oaddr = tmem + lane_addr + C::o_col(mt);
                         finish_row(R, lse2, [&](int blk, float (&f)[32]) {
                             uint32_t v[32];
                             tmem_ld_x32(oaddr + blk * 32, v);
@@ -926,15 +1118,15 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         });
                     }
                     tc_fence_before_sync();
-                    mbar_arrive(&ctrl->o_empty[ob]);
+                    mbar_arrive(&ctrl->o_empty);
                 } else {
                     const int slot = split_slot(total, n_ctas, blockIdx.x, w.ustart);
                     for (int mt = 0; mt < NUM_MT; ++mt) {
                         const int R = mt * 128 + r;
-                        const float2 st = stats[ob * 256 + R];
+                        const float2 st = stats[R];
                         const float lse2 = st.y > 0.f ? st.x + lg2(st.y) : neg_inf();
                         const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
-                        const uint32_t oaddr = tmem + lane_addr + C::o_col(mt, ob);
+                        const uint32_t oaddr = tmem + lane_addr + C::o_col(mt);
                         const bool valid = R / G < x.ntok;
                         float* po = p.part_o + ((size_t)slot * kMaxUnitRows + R) * 128;
 #pragma unroll 1
@@ -955,7 +1147,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         if (valid) p.part_lse[(size_t)slot * kMaxUnitRows + R] = lse2;
                     }
                     tc_fence_before_sync();
-                    mbar_arrive(&ctrl->o_empty[ob]);
+                    mbar_arrive(&ctrl->o_empty);
                     __threadfence();
                     named_bar_sync(1, 128);
                     const int c_first = split_owner(total, n_ctas, w.ustart);
@@ -1010,6 +1202,16 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     }
                 }
                 if (et == 0) CPA_TRACE_EVENT(8, w.seg);
+                // Q of the unit two ahead goes into the buffer this unit used: every
+                // MMA of this unit is done (o_full), so nothing reads it any more
+                if (C::kQInTmem && wq.left > 0) {
+                    const Unit xq = get_unit(p, wq.u);
+                    int qjb, qje;
+                    wq.piece(xq, qjb, qje);
+                    load_q(xq, q_loaded % 2);
+                    ++q_loaded;
+                    wq.next(xq, qjb, qje);
+                }
                 w.next(x, jb, je);
             }
         }
@@ -1017,6 +1219,12 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+#ifdef CPA_TRACE
+    if (threadIdx.x == 0 && cpa_trace_buf && blockIdx.x < 4) {
+        cpa_trace_buf[(blockIdx.x * 64 + 13) * 1024 + 1002] = clock64();
+        cpa_trace_buf[(blockIdx.x * 64 + 13) * 1024 + 1003] = globaltimer_ns();
+    }
+#endif
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, C::kTmemCols);

@@ -13,8 +13,8 @@
 
 namespace cpa {
 
-// Keys per pipeline tile (one TMA stage, one N=64 QK^T MMA).
-constexpr int kBN = 64;
+// Keys per pipeline tile (one TMA stage, one N=128 QK^T MMA).
+constexpr int kBN = 128;
 // Draft tokens per branch of a verify unit (one draft tile holds every branch).
 constexpr int kMaxDraft = 16;
 // Rows of the partial-result slots (two 128-row M tiles).

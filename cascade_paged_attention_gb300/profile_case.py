@@ -31,6 +31,8 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override B")
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--graph", action="store_true",
+                    help="also replay the iters calls from one captured CUDA graph")
     args = ap.parse_args()
 
     cpa.build_library()
@@ -86,6 +88,19 @@ def main():
     e.record()
     torch.cuda.synchronize()
     print(f"{args.case} {work}: {s.elapsed_time(e) / args.iters * 1e3:.1f} us/call")
+    if args.graph:
+        # the same calls without host gaps between them: the kernel time alone
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(args.iters):
+                call()
+        g.replay()
+        torch.cuda.synchronize()
+        s.record()
+        g.replay()
+        e.record()
+        torch.cuda.synchronize()
+        print(f"{args.case} {work}: {s.elapsed_time(e) / args.iters * 1e3:.1f} us/call (graph)")
 
 
 if __name__ == "__main__":
