@@ -906,46 +906,44 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                 l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
                                 continue;
                             }
-                            uint32_t sr[64];
-                            tmem_ld_x64(s_addr + c0, sr);
+                            // masked columns and/or the residual (the unit's last tile:
+                            // what the bf16 rounding of P dropped, itself in bf16, for a
+                            // second PV pass).  The same two pieces; a piece's residual
+                            // goes to columns 32.. of the chunk, which hold S of the second
+                            // piece, so it is stored once that piece has been read.
                             float s4[4] = {0.f, 0.f, 0.f, 0.f};
-                            uint32_t pk[32];
+                            uint32_t rk0[16];
+#pragma unroll 1
+                            for (int sc = 0; sc < 2; ++sc) {
+                                uint32_t sv[32], pk[16], rk[16];
+                                tmem_ld_x32(s_addr + (uint32_t)(c0 + 32 * sc), sv);
 #pragma unroll
-                            for (int c = 0; c < 32; ++c) {
-                                const int ca = c0 + 2 * c;
-                                float xa = __uint_as_float(sr[2 * c]);
-                                float xb = __uint_as_float(sr[2 * c + 1]);
-                                if (!whole) {
+                                for (int c = 0; c < 16; ++c) {
+                                    const int ca = c0 + 32 * sc + 2 * c;
+                                    float xa = __uint_as_float(sv[2 * c]);
+                                    float xb = __uint_as_float(sv[2 * c + 1]);
                                     if (ca < lo_c || ca >= hi_c) xa = neg_inf();
                                     if (ca + 1 < lo_c || ca + 1 >= hi_c) xb = neg_inf();
-                                }
-                                const float a = ex2(fmaf(xa, p.scale_log2, -mref));
-                                const float b = ex2(fmaf(xb, p.scale_log2, -mref));
-                                s4[c & 3] += a + b;
-                                pk[c] = pack_bf16x2(a, b);
-                            }
-                            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                            if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(16, g);
-                            tmem_st_x32(s_addr + (uint32_t)c0, pk);
-                            if (resid) {
-                                // the unit's last tile: also store what the bf16 rounding
-                                // of P dropped (itself in bf16) for a second PV pass
-#pragma unroll
-                                for (int c = 0; c < 32; ++c) {
-                                    const int ca = c0 + 2 * c;
-                                    float xa = __uint_as_float(sr[2 * c]);
-                                    float xb = __uint_as_float(sr[2 * c + 1]);
-                                    if (!whole) {
-                                        if (ca < lo_c || ca >= hi_c) xa = neg_inf();
-                                        if (ca + 1 < lo_c || ca + 1 >= hi_c) xb = neg_inf();
-                                    }
                                     const float a = ex2(fmaf(xa, p.scale_log2, -mref));
                                     const float b = ex2(fmaf(xb, p.scale_log2, -mref));
-                                    pk[c] = pack_bf16x2(a - __uint_as_float(pk[c] << 16),
+                                    s4[c & 3] += a + b;
+                                    pk[c] = pack_bf16x2(a, b);
+                                    rk[c] = pack_bf16x2(a - __uint_as_float(pk[c] << 16),
                                                         b - __uint_as_float(pk[c] & 0xFFFF0000u));
                                 }
-                                tmem_st_x32(s_addr + (uint32_t)c0 + 32, pk);
+                                tmem_st_x16_nowait(s_addr + (uint32_t)(c0 + 16 * sc), pk);
+                                if (resid) {
+                                    if (sc == 0) {
+#pragma unroll
+                                        for (int c = 0; c < 16; ++c) rk0[c] = rk[c];
+                                    } else {
+                                        tmem_st_x16_nowait(s_addr + (uint32_t)(c0 + 32), rk0);
+                                        tmem_st_x16_nowait(s_addr + (uint32_t)(c0 + 48), rk);
+                                    }
+                                }
                             }
+                            tmem_wait_st();
+                            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
                         }
                     }
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(5, g);
