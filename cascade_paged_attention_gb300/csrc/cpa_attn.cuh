@@ -213,6 +213,7 @@ struct Ctrl {
     uint64_t s_full[2], p_full[2], p_empty[2];
     uint64_t o_full, o_empty, stats_full;
     uint64_t mma_done;
+    uint64_t merge_full;  // other CTAs' parts of a split unit staged for the merge
     uint32_t tmem_base;
     uint32_t abort_flag;
     int64_t total;   // tiles of the whole problem
@@ -464,6 +465,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
         mbar_init(&ctrl->o_empty, 128);
         mbar_init(&ctrl->stats_full, 128 * NUM_MT);
         mbar_init(&ctrl->mma_done, 1);
+        mbar_init(&ctrl->merge_full, 1);
         ctrl->abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&p.kmap);
@@ -815,8 +817,9 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                             float m4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
                             if (lo_c <= c0 && hi_c >= c0 + 64) {
 #pragma unroll
-                                for (int c = 0; c < 64; ++c)
-                                    m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+                                for (int c = 0; c < 32; ++c)
+                                    m4[c & 3] = fmax3(m4[c & 3], __uint_as_float(sr[2 * c]),
+                                                      __uint_as_float(sr[2 * c + 1]));
                             } else {
 #pragma unroll
                                 for (int c = 0; c < 64; ++c)
@@ -829,10 +832,11 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(13, g);
                     if (lane == 0) CPA_TRACE_EVENT(28 + warp - C::kSmWarp0, g);
                     if (C::kSplit == 2) {
-                        // swap partial maxima with the other half of the row; the barrier
-                        // also makes the timeout decision common to all 256 threads
+                        // swap partial maxima with the warp holding the other half of the
+                        // same rows (a barrier of just that pair); it also makes the
+                        // timeout decision common to both
                         xchg[((int)(g & 1) * 2 + half) * 128 + r] = tmax_raw;
-                        okl = bar_and(2, 256, okl);
+                        okl = bar_and(4 + quarter, 64, okl);
                         tmax_raw = fmaxf(tmax_raw, xchg[((int)(g & 1) * 2 + (half ^ 1)) * 128 + r]);
                     }
                     if (!okl) {
@@ -886,22 +890,27 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                             if (__all_sync(0xffffffffu, whole && !resid)) {
                                 // every column visible, no residual: two 32-column pieces,
                                 // each one's P stored over S columns already read
+                                // (the second piece's load overlaps the first piece's math)
                                 float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                                for (int sc = 0; sc < 2; ++sc) {
-                                    uint32_t sv[32], pk[16];
-                                    tmem_ld_x32(s_addr + (uint32_t)(c0 + 32 * sc), sv);
+                                uint32_t sv[32], sw[32];
+                                tmem_ld_x32(s_addr + (uint32_t)c0, sv);
+                                tmem_ld_x32_nowait(s_addr + (uint32_t)(c0 + 32), sw);
+                                auto piece = [&](const uint32_t (&x)[32], int sc) {
+                                    uint32_t pk[16];
 #pragma unroll
                                     for (int c = 0; c < 16; ++c) {
                                         const float a =
-                                            ex2(fmaf(__uint_as_float(sv[2 * c]), p.scale_log2, -mref));
+                                            ex2(fmaf(__uint_as_float(x[2 * c]), p.scale_log2, -mref));
                                         const float b = ex2(
-                                            fmaf(__uint_as_float(sv[2 * c + 1]), p.scale_log2, -mref));
+                                            fmaf(__uint_as_float(x[2 * c + 1]), p.scale_log2, -mref));
                                         s4[c & 3] += a + b;
                                         pk[c] = pack_bf16x2(a, b);
                                     }
                                     tmem_st_x16_nowait(s_addr + (uint32_t)(c0 + 16 * sc), pk);
-                                }
+                                };
+                                piece(sv, 0);
+                                tmem_wait_ld(sw);
+                                piece(sw, 1);
                                 tmem_wait_st();
                                 l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
                                 continue;
@@ -1118,75 +1127,170 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     tc_fence_before_sync();
                     mbar_arrive(&ctrl->o_empty);
                 } else {
-                    const int slot = split_slot(total, n_ctas, blockIdx.x, w.ustart);
-                    for (int mt = 0; mt < NUM_MT; ++mt) {
-                        const int R = mt * 128 + r;
-                        const float2 st = stats[R];
-                        const float lse2 = st.y > 0.f ? st.x + lg2(st.y) : neg_inf();
-                        const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
-                        const uint32_t oaddr = tmem + lane_addr + C::o_col(mt);
-                        const bool valid = R / G < x.ntok;
-                        float* po = p.part_o + ((size_t)slot * kMaxUnitRows + R) * 128;
+                    // A unit split over CTAs c_first..c_last: the piece that finishes last
+                    // merges all pieces, in CTA order, so the result does not depend on
+                    // which one that is.  A piece that finds every other piece already
+                    // stored is that last one and takes its own part straight from TMEM;
+                    // otherwise it stores its part (O / l and its log-sum-exp) and counts
+                    // itself in, and the piece that completes the count merges.
+                    const int c_first = split_owner(total, n_ctas, w.ustart);
+                    const int c_last = split_owner(total, n_ctas, w.ustart + x.n_tiles - 1);
+                    const int np = c_last - c_first + 1;
+                    const int own = (int)blockIdx.x - c_first;
+                    // (only as the CTA's final piece: a merge holds O in TMEM, and any
+                    // later unit of this CTA waits for it)
+                    const bool final_piece = w.left == (long long)(je - jb);
+                    if (et == 0) {
+                        const unsigned seen =
+                            final_piece ? atomicAdd(p.counters + w.u, 0u) : 0u;
+                        ctrl->flag = (final_piece && seen == (unsigned)(np - 1)) ? 2 : 0;
+                    }
+                    named_bar_sync(1, 128);
+                    int mode = *reinterpret_cast<volatile int*>(&ctrl->flag);
+                    if (mode == 0) {
+                        const int slot = split_slot(total, n_ctas, blockIdx.x, w.ustart);
+                        for (int mt = 0; mt < NUM_MT; ++mt) {
+                            const int R = mt * 128 + r;
+                            const float2 st = stats[R];
+                            const float lse2 = st.y > 0.f ? st.x + lg2(st.y) : neg_inf();
+                            const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
+                            const uint32_t oaddr = tmem + lane_addr + C::o_col(mt);
+                            const bool valid = R / G < x.ntok;
+                            // float4 group q of every row side by side: a warp's store
+                            // of one group covers 512 contiguous bytes
+                            float4* po = reinterpret_cast<float4*>(p.part_o) +
+                                         (size_t)slot * 32 * kMaxUnitRows + R;
 #pragma unroll 1
-                        for (int blk = 0; blk < 4; ++blk) {
-                            uint32_t v[32];
-                            __syncwarp();
-                            tmem_ld_x32(oaddr + blk * 32, v);
-                            if (valid) {
-                                float4* d4 = reinterpret_cast<float4*>(po + blk * 32);
+                            for (int blk = 0; blk < 4; ++blk) {
+                                uint32_t v[32];
+                                __syncwarp();
+                                tmem_ld_x32(oaddr + blk * 32, v);
+                                if (valid) {
 #pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    d4[e] = make_float4(__uint_as_float(v[4 * e]) * inv,
+                                    for (int e = 0; e < 8; ++e)
+                                        po[(blk * 8 + e) * kMaxUnitRows] =
+                                            make_float4(__uint_as_float(v[4 * e]) * inv,
                                                         __uint_as_float(v[4 * e + 1]) * inv,
                                                         __uint_as_float(v[4 * e + 2]) * inv,
                                                         __uint_as_float(v[4 * e + 3]) * inv);
+                                }
+                            }
+                            if (valid) p.part_lse[(size_t)slot * kMaxUnitRows + R] = lse2;
+                        }
+                        if (et == 0) CPA_TRACE_EVENT(52, w.seg);
+                        tc_fence_before_sync();
+                        mbar_arrive(&ctrl->o_empty);
+                        __threadfence();
+                        named_bar_sync(1, 128);
+                        if (et == 0) CPA_TRACE_EVENT(53, w.seg);
+                        if (et == 0) {
+                            const unsigned old = atomicAdd(p.counters + w.u, 1u);
+                            ctrl->flag = (old == (unsigned)(np - 1)) ? 1 : 0;
+                        }
+                        named_bar_sync(1, 128);
+                        mode = *reinterpret_cast<volatile int*>(&ctrl->flag);
+                        if (et == 0) CPA_TRACE_EVENT(54, w.seg);
+                    }
+                    if (mode != 0) {
+                        // mode 2: this piece's part comes from TMEM, the others' from memory.
+                        // As the CTA's final piece every K/V stage is idle (all MMAs are
+                        // done): the other parts are bulk-copied there, one copy per float4
+                        // column group with the unit's rows side by side, so that the merge
+                        // waits on memory once instead of once per group and part.
+                        __threadfence();
+                        const int nrows = x.ntok * G;
+                        const uint32_t part_bytes = 32u * (uint32_t)nrows * 16u;
+                        const bool staged = mode == 2 && (uint32_t)(np - 1) * part_bytes <=
+                                                             (uint32_t)p.n_stages * kStageBytes;
+                        const float4* stage4 = reinterpret_cast<const float4*>(smem + p.off_kv);
+                        if (staged) {
+                            if (et < 32) {
+                                // lane q of the first epilogue warp copies column group q of
+                                // every other part (one thread's copies issue one by one)
+                                fence_proxy_async_global();
+                                if (et == 0)
+                                    mbar_arrive_expect_tx(&ctrl->merge_full,
+                                                          (uint32_t)(np - 1) * part_bytes);
+                                __syncwarp();
+                                for (int c = 0, k = 0; c < np; ++c) {
+                                    if (c == own) continue;
+                                    const float4* src =
+                                        reinterpret_cast<const float4*>(p.part_o) +
+                                        (size_t)split_slot(total, n_ctas, c_first + c, w.ustart) * 32 *
+                                            kMaxUnitRows;
+                                    bulk_load(smem + p.off_kv + ((size_t)k * 32 + et) * nrows * 16,
+                                              src + (size_t)et * kMaxUnitRows, (uint32_t)nrows * 16u,
+                                              &ctrl->merge_full);
+                                    ++k;
+                                }
+                            }
+                            // at most one staged merge per CTA: phase 0
+                            const bool okm = bar_and(1, 128, mbar_wait(&ctrl->merge_full, 0,
+                                                                       abort_flag, p.status));
+                            if (!okm) {
+                                ok = false;
+                                break;
                             }
                         }
-                        if (valid) p.part_lse[(size_t)slot * kMaxUnitRows + R] = lse2;
-                    }
-                    tc_fence_before_sync();
-                    mbar_arrive(&ctrl->o_empty);
-                    __threadfence();
-                    named_bar_sync(1, 128);
-                    const int c_first = split_owner(total, n_ctas, w.ustart);
-                    const int c_last = split_owner(total, n_ctas, w.ustart + x.n_tiles - 1);
-                    if (et == 0) {
-                        const unsigned old = atomicAdd(p.counters + w.u, 1u);
-                        ctrl->flag = (old == (unsigned)(c_last - c_first)) ? 1 : 0;
-                    }
-                    named_bar_sync(1, 128);
-                    const bool last = *reinterpret_cast<volatile int*>(&ctrl->flag) != 0;
-                    if (last) {
-                        __threadfence();
-                        const int np = c_last - c_first + 1;
+                        if (et == 0) CPA_TRACE_EVENT(55, w.seg);
                         for (int mt = 0; mt < NUM_MT; ++mt) {
                             const int R = mt * 128 + r;
                             const bool valid = R / G < x.ntok;
+                            const float2 st = stats[R];
+                            const float lse_own = st.y > 0.f ? st.x + lg2(st.y) : neg_inf();
+                            const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
+                            const uint32_t oaddr = tmem + lane_addr + C::o_col(mt);
                             auto slot_of = [&](int c) -> size_t {
-                                return (size_t)split_slot(total, n_ctas, c_first + c, w.ustart) *
-                                           kMaxUnitRows + R;
+                                return (size_t)split_slot(total, n_ctas, c_first + c, w.ustart);
                             };
-                            float mx = neg_inf();
-                            if (valid)
-                                for (int c = 0; c < np; ++c)
-                                    mx = fmaxf(mx, __ldcg(p.part_lse + slot_of(c)));
-                            float den = 0.f;
-                            if (valid && mx != neg_inf())
-                                for (int c = 0; c < np; ++c)
-                                    den += ex2(__ldcg(p.part_lse + slot_of(c)) - mx);
+                            auto lse_of = [&](int c) -> float {
+                                return (mode == 2 && c == own)
+                                           ? lse_own
+                                           : __ldcg(p.part_lse + slot_of(c) * kMaxUnitRows + R);
+                            };
+                            // log2 of the sum of 2^lse over the parts, as a running (max, sum)
+                            float mx = neg_inf(), den = 0.f;
+                            if (valid) {
+#pragma unroll 4
+                                for (int c = 0; c < np; ++c) {
+                                    const float lc = lse_of(c);
+                                    if (lc == neg_inf()) continue;
+                                    if (lc > mx) {
+                                        den = (mx == neg_inf() ? 0.f : den * ex2(mx - lc)) + 1.f;
+                                        mx = lc;
+                                    } else {
+                                        den += ex2(lc - mx);
+                                    }
+                                }
+                            }
                             const float lse2 = (den > 0.f) ? mx + lg2(den) : neg_inf();
+                            if (et == 0) CPA_TRACE_EVENT(56, w.seg);
                             finish_row(R, lse2, [&](int blk, float (&f)[32]) {
+                                uint32_t v[32];
+                                if (mode == 2) tmem_ld_x32(oaddr + blk * 32, v);
 #pragma unroll
                                 for (int e = 0; e < 32; ++e) f[e] = 0.f;
                                 if (!valid || den == 0.f) return;
                                 for (int c = 0; c < np; ++c) {
-                                    const size_t sl = slot_of(c);
-                                    const float wc = ex2(__ldcg(p.part_lse + sl) - lse2);
-                                    const float4* s4 =
-                                        reinterpret_cast<const float4*>(p.part_o + sl * 128 + blk * 32);
-                                    float4 v4[8];
+                                    const float wc = ex2(lse_of(c) - lse2);
+                                    if (mode == 2 && c == own) {
 #pragma unroll
-                                    for (int e = 0; e < 8; ++e) v4[e] = __ldcg(s4 + e);
+                                        for (int e = 0; e < 32; ++e)
+                                            f[e] = fmaf(wc, __uint_as_float(v[e]) * inv, f[e]);
+                                        continue;
+                                    }
+                                    float4 v4[8];
+                                    if (staged) {
+                                        const float4* s4 =
+                                            stage4 + ((size_t)(c < own ? c : c - 1) * 32 + blk * 8) * nrows + R;
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e) v4[e] = s4[e * nrows];
+                                    } else {
+                                        const float4* s4 = reinterpret_cast<const float4*>(p.part_o) +
+                                                           (slot_of(c) * 32 + blk * 8) * kMaxUnitRows + R;
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e) v4[e] = __ldcg(s4 + e * kMaxUnitRows);
+                                    }
 #pragma unroll
                                     for (int e = 0; e < 8; ++e) {
                                         f[4 * e] = fmaf(wc, v4[e].x, f[4 * e]);
@@ -1196,6 +1300,10 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                     }
                                 }
                             });
+                        }
+                        if (mode == 2) {
+                            tc_fence_before_sync();
+                            mbar_arrive(&ctrl->o_empty);
                         }
                     }
                 }
