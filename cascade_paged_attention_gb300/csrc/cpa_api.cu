@@ -259,8 +259,10 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
     if (!kv_maps(p, k_pages, v_pages, H_kv, num_pages, page_size)) return CPA_ERR_CUDA;
     if (draft) {
         const uint64_t rows = (uint64_t)num_pages * page_size;
-        if (!make_map(&p.kdmap, k_pages, H_kv, rows, 1, sb) ||
-            !make_map(&p.vdmap, v_pages, H_kv, rows, 1, sb))
+        // a branch's draft box is exactly its S rows: the rest of the branch block
+        // keeps earlier, finite tile data, which P = 0 there multiplies away
+        if (!make_map(&p.kdmap, k_pages, H_kv, rows, 1, S) ||
+            !make_map(&p.vdmap, v_pages, H_kv, rows, 1, S))
             return CPA_ERR_CUDA;
     }
     const long long n_units = (long long)B * p.upg;

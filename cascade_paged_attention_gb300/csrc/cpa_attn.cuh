@@ -476,6 +476,15 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
         tmem_alloc(&ctrl->tmem_base, C::kTmemCols);
         tmem_relinquish();
     }
+    // V rows a tile does not load (past a sequence's end, past a branch's drafts)
+    // keep what an earlier tile left there; zero every V stage once so that this
+    // is always finite data, which P = 0 multiplies away
+    for (int i = threadIdx.x; i < p.n_stages * 2 * kBN * 8; i += blockDim.x) {
+        const int st = i / (2 * kBN * 8), rem = i % (2 * kBN * 8);
+        *reinterpret_cast<uint4*>(smem + p.off_kv + st * kStageBytes + 2 * kBN * 128 + rem * 16) =
+            make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -559,7 +568,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         const uint32_t mask = __ballot_sync(0xffffffffu, use);
                         if (lane == 0)
                             mbar_arrive_expect_tx(&ctrl->kv_full[st],
-                                                  (uint32_t)__popc(mask) * 4u * p.sb * 128u);
+                                                  (uint32_t)__popc(mask) * 4u * p.S * 128u);
                         __syncwarp();
                         // every lane runs the same iterations (the shuffle needs the whole
                         // warp); only the copy itself is predicated
@@ -802,7 +811,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     }
                     if (it >= x.ntok) {
                         lo_c = 0;
-                        hi_c = kBN;
+                        hi_c = dtile ? 0 : kBN;
                     }
                     const uint32_t s_addr = tmem + lane_addr + C::s_col(mt, sb);
                     if (okl) tc_fence_after_sync();
@@ -812,19 +821,28 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
 #pragma unroll 1
                         for (int ch = 0; ch < kChunks; ++ch) {
                             const int c0 = (half + ch) * 64;
-                            uint32_t sr[64];
-                            tmem_ld_x64(s_addr + c0, sr);
                             float m4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
-                            if (lo_c <= c0 && hi_c >= c0 + 64) {
+                            if (__all_sync(0xffffffffu, lo_c <= c0 && hi_c >= c0 + 64)) {
+                                uint32_t sr[64];
+                                tmem_ld_x64(s_addr + c0, sr);
 #pragma unroll
                                 for (int c = 0; c < 32; ++c)
                                     m4[c & 3] = fmax3(m4[c & 3], __uint_as_float(sr[2 * c]),
                                                       __uint_as_float(sr[2 * c + 1]));
                             } else {
+                                // 32-column pieces; one that no row of the warp sees is
+                                // not even read
+#pragma unroll 1
+                                for (int pc = 0; pc < 2; ++pc) {
+                                    const int a = c0 + 32 * pc;
+                                    if (!__any_sync(0xffffffffu, lo_c < a + 32 && hi_c > a)) continue;
+                                    uint32_t sv[32];
+                                    tmem_ld_x32(s_addr + a, sv);
 #pragma unroll
-                                for (int c = 0; c < 64; ++c)
-                                    if (c0 + c >= lo_c && c0 + c < hi_c)
-                                        m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+                                    for (int c = 0; c < 32; ++c)
+                                        if (a + c >= lo_c && a + c < hi_c)
+                                            m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c]));
+                                }
                             }
                             tmax_raw = fmaxf(tmax_raw, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
                         }
@@ -925,7 +943,14 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
 #pragma unroll 1
                             for (int sc = 0; sc < 2; ++sc) {
                                 uint32_t sv[32], pk[16], rk[16];
-                                tmem_ld_x32(s_addr + (uint32_t)(c0 + 32 * sc), sv);
+                                const int a0 = c0 + 32 * sc;
+                                if (__any_sync(0xffffffffu, lo_c < a0 + 32 && hi_c > a0)) {
+                                    tmem_ld_x32(s_addr + (uint32_t)a0, sv);
+                                } else {
+                                    // no row of the warp sees this piece: P = 0 throughout
+#pragma unroll
+                                    for (int c = 0; c < 32; ++c) sv[c] = __float_as_uint(neg_inf());
+                                }
 #pragma unroll
                                 for (int c = 0; c < 16; ++c) {
                                     const int ca = c0 + 32 * sc + 2 * c;
@@ -958,28 +983,16 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(5, g);
                     if (lane == 0) CPA_TRACE_EVENT(44 + warp - C::kSmWarp0, g);
                     bool zeroed = false;
-                    if (wgi == 0 && dtile) {
-                        // rows of the draft tile that hold no draft (slots past S of a
-                        // branch's page, blocks past the last branch): zero their V so
-                        // that P = 0 there contributes exactly nothing
-                        const int st = (int)(g % p.n_stages);
-                        uint8_t* vb = smem + p.off_kv + st * kStageBytes + 2 * kBN * 128;
-                        for (int i = r; i < 2 * kBN * 8; i += 128) {
-                            const int hh = i / (kBN * 8), row = (i / 8) % kBN;
-                            if (row >= p.nbr * p.sb || (row % p.sb) >= p.S)
-                                *reinterpret_cast<uint4*>(vb + hh * kBN * 128 + row * 128 +
-                                                          (i % 8) * 16) = make_uint4(0, 0, 0, 0);
-                        }
-                        zeroed = true;
-                    } else if (wgi == 0 && key0 + kBN > x.valid_end) {
-                        // V rows past the sequence end hold whatever the page had (or stale
-                        // data): zero them so that P = 0 there contributes exactly nothing
+                    if (wgi == 0 && !dtile && key0 + kBN > x.valid_end && x.valid_end % p.boxr != 0) {
+                        // the box holding the sequence's last key was loaded whole: zero
+                        // its V rows past the end (whatever the page holds there), so that
+                        // P = 0 contributes exactly nothing
                         const int first = max(0, x.valid_end - key0);
+                        const int stop = min(kBN, (first / p.boxr + 1) * p.boxr);
                         const int st = (int)(g % p.n_stages);
                         uint8_t* vb = smem + p.off_kv + st * kStageBytes + 2 * kBN * 128;
-                        const int n16 = (kBN - first) * 8;  // 16-B chunks per half
-                        for (int i = r; i < 2 * n16; i += 128) {
-                            const int hh = i / n16, rem = i % n16;
+                        for (int i = r; i < 2 * (stop - first) * 8; i += 128) {
+                            const int hh = i & 1, rem = i >> 1;  // rem: 16-B chunk within the rows
                             *reinterpret_cast<uint4*>(vb + hh * kBN * 128 + first * 128 + rem * 16) =
                                 make_uint4(0, 0, 0, 0);
                         }
