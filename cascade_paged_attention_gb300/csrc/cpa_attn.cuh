@@ -40,6 +40,7 @@
 // applies the causal-within-branch mask, so Pass B and its merge with Pass A
 // run inside the same online softmax on the tensor cores.
 #pragma once
+#include <type_traits>
 #include <cstdint>
 
 #include "cpa_device.cuh"
@@ -942,28 +943,36 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                             uint32_t rk0[16];
 #pragma unroll 1
                             for (int sc = 0; sc < 2; ++sc) {
-                                uint32_t sv[32], pk[16], rk[16];
+                                uint32_t pk[16], rk[16];
                                 const int a0 = c0 + 32 * sc;
-                                if (__any_sync(0xffffffffu, lo_c < a0 + 32 && hi_c > a0)) {
+                                // P (and its residual) of keys a0 .. a0+31, with masks
+                                auto masked = [&](auto with_resid) {
+                                    uint32_t sv[32];
                                     tmem_ld_x32(s_addr + (uint32_t)a0, sv);
-                                } else {
+#pragma unroll
+                                    for (int c = 0; c < 16; ++c) {
+                                        const int ca = a0 + 2 * c;
+                                        float xa = __uint_as_float(sv[2 * c]);
+                                        float xb = __uint_as_float(sv[2 * c + 1]);
+                                        if (ca < lo_c || ca >= hi_c) xa = neg_inf();
+                                        if (ca + 1 < lo_c || ca + 1 >= hi_c) xb = neg_inf();
+                                        const float a = ex2(fmaf(xa, p.scale_log2, -mref));
+                                        const float b = ex2(fmaf(xb, p.scale_log2, -mref));
+                                        s4[c & 3] += a + b;
+                                        pk[c] = pack_bf16x2(a, b);
+                                        if constexpr (decltype(with_resid)::value)
+                                            rk[c] = pack_bf16x2(a - __uint_as_float(pk[c] << 16),
+                                                                b - __uint_as_float(pk[c] & 0xFFFF0000u));
+                                    }
+                                };
+                                if (!__any_sync(0xffffffffu, lo_c < a0 + 32 && hi_c > a0)) {
                                     // no row of the warp sees this piece: P = 0 throughout
 #pragma unroll
-                                    for (int c = 0; c < 32; ++c) sv[c] = __float_as_uint(neg_inf());
-                                }
-#pragma unroll
-                                for (int c = 0; c < 16; ++c) {
-                                    const int ca = c0 + 32 * sc + 2 * c;
-                                    float xa = __uint_as_float(sv[2 * c]);
-                                    float xb = __uint_as_float(sv[2 * c + 1]);
-                                    if (ca < lo_c || ca >= hi_c) xa = neg_inf();
-                                    if (ca + 1 < lo_c || ca + 1 >= hi_c) xb = neg_inf();
-                                    const float a = ex2(fmaf(xa, p.scale_log2, -mref));
-                                    const float b = ex2(fmaf(xb, p.scale_log2, -mref));
-                                    s4[c & 3] += a + b;
-                                    pk[c] = pack_bf16x2(a, b);
-                                    rk[c] = pack_bf16x2(a - __uint_as_float(pk[c] << 16),
-                                                        b - __uint_as_float(pk[c] & 0xFFFF0000u));
+                                    for (int c = 0; c < 16; ++c) pk[c] = rk[c] = 0u;
+                                } else if (resid) {
+                                    masked(std::true_type{});
+                                } else {
+                                    masked(std::false_type{});
                                 }
                                 tmem_st_x16_nowait(s_addr + (uint32_t)(c0 + 16 * sc), pk);
                                 if (resid) {
