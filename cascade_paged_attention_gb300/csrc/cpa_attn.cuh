@@ -1170,6 +1170,9 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     named_bar_sync(1, 128);
                     int mode = *reinterpret_cast<volatile int*>(&ctrl->flag);
                     if (mode == 0) {
+                        // the part stays in L2 until the merging CTA reads it, typically
+                        // at the very end, after the whole K/V stream has passed through
+                        const uint64_t pol_keep = l2_policy_evict_last();
                         const int slot = split_slot(total, n_ctas, blockIdx.x, w.ustart);
                         for (int mt = 0; mt < NUM_MT; ++mt) {
                             const int R = mt * 128 + r;
@@ -1190,11 +1193,12 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                 if (valid) {
 #pragma unroll
                                     for (int e = 0; e < 8; ++e)
-                                        po[(blk * 8 + e) * kMaxUnitRows] =
-                                            make_float4(__uint_as_float(v[4 * e]) * inv,
-                                                        __uint_as_float(v[4 * e + 1]) * inv,
-                                                        __uint_as_float(v[4 * e + 2]) * inv,
-                                                        __uint_as_float(v[4 * e + 3]) * inv);
+                                        st_global_hint(po + (blk * 8 + e) * kMaxUnitRows,
+                                                       make_float4(__uint_as_float(v[4 * e]) * inv,
+                                                                   __uint_as_float(v[4 * e + 1]) * inv,
+                                                                   __uint_as_float(v[4 * e + 2]) * inv,
+                                                                   __uint_as_float(v[4 * e + 3]) * inv),
+                                                       pol_keep);
                                 }
                             }
                             if (valid) p.part_lse[(size_t)slot * kMaxUnitRows + R] = lse2;
@@ -1221,10 +1225,13 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         // waits on memory once instead of once per group and part.
                         __threadfence();
                         const int nrows = x.ntok * G;
+                        const int nl = (nrows + 3) & ~3;  // log-sum-exp entries copied per part
                         const uint32_t part_bytes = 32u * (uint32_t)nrows * 16u;
-                        const bool staged = mode == 2 && (uint32_t)(np - 1) * part_bytes <=
+                        const uint32_t lse_off = (uint32_t)(np - 1) * part_bytes;
+                        const bool staged = mode == 2 && lse_off + (uint32_t)(np - 1) * nl * 4u <=
                                                              (uint32_t)p.n_stages * kStageBytes;
                         const float4* stage4 = reinterpret_cast<const float4*>(smem + p.off_kv);
+                        const float* stage_lse = reinterpret_cast<const float*>(smem + p.off_kv + lse_off);
                         if (staged) {
                             if (et < 32) {
                                 // lane q of the first epilogue warp copies column group q of
@@ -1232,17 +1239,20 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                 fence_proxy_async_global();
                                 if (et == 0)
                                     mbar_arrive_expect_tx(&ctrl->merge_full,
-                                                          (uint32_t)(np - 1) * part_bytes);
+                                                          lse_off + (uint32_t)(np - 1) * nl * 4u);
                                 __syncwarp();
                                 for (int c = 0, k = 0; c < np; ++c) {
                                     if (c == own) continue;
+                                    const size_t sl = split_slot(total, n_ctas, c_first + c, w.ustart);
                                     const float4* src =
-                                        reinterpret_cast<const float4*>(p.part_o) +
-                                        (size_t)split_slot(total, n_ctas, c_first + c, w.ustart) * 32 *
-                                            kMaxUnitRows;
+                                        reinterpret_cast<const float4*>(p.part_o) + sl * 32 * kMaxUnitRows;
                                     bulk_load(smem + p.off_kv + ((size_t)k * 32 + et) * nrows * 16,
                                               src + (size_t)et * kMaxUnitRows, (uint32_t)nrows * 16u,
                                               &ctrl->merge_full);
+                                    if (et == 0)
+                                        bulk_load(smem + p.off_kv + lse_off + (size_t)k * nl * 4,
+                                                  p.part_lse + sl * kMaxUnitRows, (uint32_t)nl * 4u,
+                                                  &ctrl->merge_full);
                                     ++k;
                                 }
                             }
@@ -1266,9 +1276,9 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                 return (size_t)split_slot(total, n_ctas, c_first + c, w.ustart);
                             };
                             auto lse_of = [&](int c) -> float {
-                                return (mode == 2 && c == own)
-                                           ? lse_own
-                                           : __ldcg(p.part_lse + slot_of(c) * kMaxUnitRows + R);
+                                if (mode == 2 && c == own) return lse_own;
+                                if (staged) return stage_lse[(c < own ? c : c - 1) * nl + R];
+                                return __ldcg(p.part_lse + slot_of(c) * kMaxUnitRows + R);
                             };
                             // log2 of the sum of 2^lse over the parts, as a running (max, sum)
                             float mx = neg_inf(), den = 0.f;

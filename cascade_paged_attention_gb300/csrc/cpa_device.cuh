@@ -167,6 +167,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// 16-byte global store with an L2 eviction-priority hint.
+__device__ __forceinline__ void st_global_hint(float4* ptr, const float4& v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
+                 : "memory");
+}
+
 // Plain (non-tensor) bulk copy of `bytes` (multiple of 16, both ends 16-B aligned).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
