@@ -115,6 +115,7 @@ struct Unit {
     int tile_base;    // first key tile
     int n_prefix;     // prefix tiles; tile n_prefix (verify) holds the unit's drafts
     int n_tiles;
+    int resid_tile;   // tile that also sends P's bf16 residual through PV, or -1
     const int32_t* trow;
 };
 
@@ -163,6 +164,13 @@ __device__ __forceinline__ int verify_unit_tiles(const AttnParams& p, int L) {
     return verify_prefix_tiles(p, L) + (p.has_draft ? 1 : 0);
 }
 
+// P goes through the tensor cores in bf16.  Over many keys its rounding errors
+// average out; when a unit has few keys they do not, and the output would carry
+// up to 2^-9 of |v| on top of its own bf16 rounding.  So a small unit's last
+// tile (the one holding every key of the rows that see the fewest) also sends
+// what the rounding dropped, itself in bf16, through a second PV pass.
+constexpr int kResidMaxKeys = 512;
+
 __device__ __forceinline__ Unit get_unit(const AttnParams& p, int u) {
     Unit x;
     if (is_verify(p.mode)) {
@@ -204,8 +212,10 @@ __device__ __forceinline__ Unit get_unit(const AttnParams& p, int u) {
         x.n_prefix = x.n_tiles;
         x.trow = p.ptab + (size_t)x.b * p.ptab_stride;
     }
+    x.resid_tile = (x.hi - x.lo) + (p.has_draft ? p.S : 0) <= kResidMaxKeys ? x.n_tiles - 1 : -1;
     return x;
 }
+
 
 // ------------------------------------------------------------------ shared control block
 struct Ctrl {
@@ -698,7 +708,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                             const int st = (int)(gp % p.n_stages);
                             const uint32_t vb = sbase + p.off_kv + st * kStageBytes + 2 * kBN * 128;
                             const bool first = cp.first();
-                            const int passes = (cp.jj == cp.x.n_tiles - 1) ? 2 : 1;
+                            const int passes = cp.jj == cp.x.resid_tile ? 2 : 1;
                             for (int mt = 0; mt < NUM_MT; ++mt) {
                                 // P of keys 64c..64c+63 (bf16, two per column) sits in the
                                 // first 32 of the 64 S columns those keys came from, its
@@ -816,37 +826,40 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     }
                     const uint32_t s_addr = tmem + lane_addr + C::s_col(mt, sb);
                     if (okl) tc_fence_after_sync();
+                    // Both passes walk this thread's columns in 32-column pieces.  A piece
+                    // is, for the whole warp, unseen (no row sees any of it: not read, P = 0),
+                    // whole (every row sees all of it) or partial (masked first).  Every tile
+                    // runs the same per-piece code, so the rare masked tiles at a unit's end
+                    // find it already in the instruction cache; only the masking is extra.
+                    auto piece_class = [&](int a) -> int {  // 0 unseen, 1 partial, 2 whole
+                        if (!__any_sync(0xffffffffu, lo_c < a + 32 && hi_c > a)) return 0;
+                        return __all_sync(0xffffffffu, lo_c <= a && hi_c >= a + 32) ? 2 : 1;
+                    };
+                    auto mask_piece = [&](uint32_t (&v)[32], int a) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (a + c < lo_c || a + c >= hi_c) v[c] = __float_as_uint(neg_inf());
+                    };
                     // pass 1: this thread's raw maximum over its columns
                     float tmax_raw = neg_inf();
                     if (okl && !warp_inert) {
+                        float m4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
 #pragma unroll 1
-                        for (int ch = 0; ch < kChunks; ++ch) {
-                            const int c0 = (half + ch) * 64;
-                            float m4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
-                            if (__all_sync(0xffffffffu, lo_c <= c0 && hi_c >= c0 + 64)) {
-                                uint32_t sr[64];
-                                tmem_ld_x64(s_addr + c0, sr);
+                        for (int pc = 0; pc < 2 * kChunks; ++pc) {
+                            const int a = half * 64 + (pc >> 1) * 64 * C::kSplit + (pc & 1) * 32;
+                            const int cls = piece_class(a);
+                            if (cls == 0) continue;
+                            uint32_t sv[32];
+                            tmem_ld_x32(s_addr + (uint32_t)a, sv);
+                            if (cls == 1) mask_piece(sv, a);
 #pragma unroll
-                                for (int c = 0; c < 32; ++c)
-                                    m4[c & 3] = fmax3(m4[c & 3], __uint_as_float(sr[2 * c]),
-                                                      __uint_as_float(sr[2 * c + 1]));
-                            } else {
-                                // 32-column pieces; one that no row of the warp sees is
-                                // not even read
-#pragma unroll 1
-                                for (int pc = 0; pc < 2; ++pc) {
-                                    const int a = c0 + 32 * pc;
-                                    if (!__any_sync(0xffffffffu, lo_c < a + 32 && hi_c > a)) continue;
-                                    uint32_t sv[32];
-                                    tmem_ld_x32(s_addr + a, sv);
-#pragma unroll
-                                    for (int c = 0; c < 32; ++c)
-                                        if (a + c >= lo_c && a + c < hi_c)
-                                            m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c]));
-                                }
-                            }
-                            tmax_raw = fmaxf(tmax_raw, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                            for (int c = 0; c < 8; ++c)
+                                m4[c & 3] = fmax3(m4[c & 3], fmax3(__uint_as_float(sv[4 * c]),
+                                                                   __uint_as_float(sv[4 * c + 1]),
+                                                                   __uint_as_float(sv[4 * c + 2])),
+                                                  __uint_as_float(sv[4 * c + 3]));
                         }
+                        tmax_raw = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                     }
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(13, g);
                     if (lane == 0) CPA_TRACE_EVENT(28 + warp - C::kSmWarp0, g);
@@ -897,85 +910,74 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(17, g);
                         if (m_used == neg_inf()) m_used = tmax;
                         const float mref = (m_used == neg_inf()) ? 0.f : m_used;
-                        const bool resid = jj == x.n_tiles - 1;
-                        // pass 2: P = 2^(s*scale - mref) in bf16 over the S columns it came
-                        // from, inside the chunk's own 64 columns, so no chunk's P lands on
-                        // S another thread or chunk has yet to read (the MMA that produced
-                        // S is done, and so is every earlier MMA: no PV still reads them)
-#pragma unroll 1
-                        for (int ch = 0; ch < kChunks; ++ch) {
-                            const int c0 = (half + ch) * 64;
-                            const bool whole = lo_c <= c0 && hi_c >= c0 + 64;
-                            if (__all_sync(0xffffffffu, whole && !resid)) {
-                                // every column visible, no residual: two 32-column pieces,
-                                // each one's P stored over S columns already read
-                                // (the second piece's load overlaps the first piece's math)
-                                float s4[4] = {0.f, 0.f, 0.f, 0.f};
-                                uint32_t sv[32], sw[32];
-                                tmem_ld_x32(s_addr + (uint32_t)c0, sv);
-                                tmem_ld_x32_nowait(s_addr + (uint32_t)(c0 + 32), sw);
-                                auto piece = [&](const uint32_t (&x)[32], int sc) {
-                                    uint32_t pk[16];
+                        const bool resid = jj == x.resid_tile;
+                        // pass 2: P = 2^(s*scale - mref) in bf16, written over the S columns
+                        // it came from: piece k of a 64-column chunk puts its P in columns
+                        // 16k..16k+15 of the chunk (S there is already read).  (The MMA that
+                        // produced S is done, and so is every earlier MMA: no PV still reads
+                        // these columns.)
+                        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                        auto exp_piece = [&](const uint32_t (&sv)[32], uint32_t (&pk)[16]) {
 #pragma unroll
-                                    for (int c = 0; c < 16; ++c) {
-                                        const float a =
-                                            ex2(fmaf(__uint_as_float(x[2 * c]), p.scale_log2, -mref));
-                                        const float b = ex2(
-                                            fmaf(__uint_as_float(x[2 * c + 1]), p.scale_log2, -mref));
-                                        s4[c & 3] += a + b;
-                                        pk[c] = pack_bf16x2(a, b);
+                            for (int c = 0; c < 16; ++c) {
+                                const float ea =
+                                    ex2(fmaf(__uint_as_float(sv[2 * c]), p.scale_log2, -mref));
+                                const float eb =
+                                    ex2(fmaf(__uint_as_float(sv[2 * c + 1]), p.scale_log2, -mref));
+                                s4[c & 3] += ea + eb;
+                                pk[c] = pack_bf16x2(ea, eb);
+                            }
+                        };
+                        if (!resid) {
+#pragma unroll 1
+                            for (int pc = 0; pc < 2 * kChunks; ++pc) {
+                                const int c0 = half * 64 + (pc >> 1) * 64 * C::kSplit;
+                                const int a = c0 + 32 * (pc & 1);
+                                const int cls = piece_class(a);
+                                uint32_t pk[16];
+                                if (cls == 0) {
+#pragma unroll
+                                    for (int c = 0; c < 16; ++c) pk[c] = 0u;
+                                } else {
+                                    uint32_t sv[32];
+                                    tmem_ld_x32(s_addr + (uint32_t)a, sv);
+                                    if (cls == 1) mask_piece(sv, a);
+                                    exp_piece(sv, pk);
+                                }
+                                tmem_st_x16_nowait(s_addr + (uint32_t)(c0 + 16 * (pc & 1)), pk);
+                            }
+                        } else {
+                            // a small unit's last tile: the bf16 residual of P (what the
+                            // rounding dropped) goes to columns 32.. of the chunk, which
+                            // hold the second piece's S, so it is written once that piece
+                            // has been read
+#pragma unroll 1
+                            for (int ch = 0; ch < kChunks; ++ch) {
+                                const int c0 = (half + ch) * 64;
+                                uint32_t rk0[16];
+#pragma unroll 1
+                                for (int sc = 0; sc < 2; ++sc) {
+                                    const int a = c0 + 32 * sc;
+                                    uint32_t pk[16], rk[16];
+                                    if (piece_class(a) == 0) {
+#pragma unroll
+                                        for (int c = 0; c < 16; ++c) pk[c] = rk[c] = 0u;
+                                    } else {
+                                        uint32_t sv[32];
+                                        tmem_ld_x32(s_addr + (uint32_t)a, sv);
+                                        mask_piece(sv, a);
+                                        exp_piece(sv, pk);
+#pragma unroll
+                                        for (int c = 0; c < 16; ++c) {
+                                            const float ea = ex2(
+                                                fmaf(__uint_as_float(sv[2 * c]), p.scale_log2, -mref));
+                                            const float eb = ex2(fmaf(__uint_as_float(sv[2 * c + 1]),
+                                                                      p.scale_log2, -mref));
+                                            rk[c] = pack_bf16x2(ea - __uint_as_float(pk[c] << 16),
+                                                                eb - __uint_as_float(pk[c] & 0xFFFF0000u));
+                                        }
                                     }
                                     tmem_st_x16_nowait(s_addr + (uint32_t)(c0 + 16 * sc), pk);
-                                };
-                                piece(sv, 0);
-                                tmem_wait_ld(sw);
-                                piece(sw, 1);
-                                tmem_wait_st();
-                                l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                                continue;
-                            }
-                            // masked columns and/or the residual (the unit's last tile:
-                            // what the bf16 rounding of P dropped, itself in bf16, for a
-                            // second PV pass).  The same two pieces; a piece's residual
-                            // goes to columns 32.. of the chunk, which hold S of the second
-                            // piece, so it is stored once that piece has been read.
-                            float s4[4] = {0.f, 0.f, 0.f, 0.f};
-                            uint32_t rk0[16];
-#pragma unroll 1
-                            for (int sc = 0; sc < 2; ++sc) {
-                                uint32_t pk[16], rk[16];
-                                const int a0 = c0 + 32 * sc;
-                                // P (and its residual) of keys a0 .. a0+31, with masks
-                                auto masked = [&](auto with_resid) {
-                                    uint32_t sv[32];
-                                    tmem_ld_x32(s_addr + (uint32_t)a0, sv);
-#pragma unroll
-                                    for (int c = 0; c < 16; ++c) {
-                                        const int ca = a0 + 2 * c;
-                                        float xa = __uint_as_float(sv[2 * c]);
-                                        float xb = __uint_as_float(sv[2 * c + 1]);
-                                        if (ca < lo_c || ca >= hi_c) xa = neg_inf();
-                                        if (ca + 1 < lo_c || ca + 1 >= hi_c) xb = neg_inf();
-                                        const float a = ex2(fmaf(xa, p.scale_log2, -mref));
-                                        const float b = ex2(fmaf(xb, p.scale_log2, -mref));
-                                        s4[c & 3] += a + b;
-                                        pk[c] = pack_bf16x2(a, b);
-                                        if constexpr (decltype(with_resid)::value)
-                                            rk[c] = pack_bf16x2(a - __uint_as_float(pk[c] << 16),
-                                                                b - __uint_as_float(pk[c] & 0xFFFF0000u));
-                                    }
-                                };
-                                if (!__any_sync(0xffffffffu, lo_c < a0 + 32 && hi_c > a0)) {
-                                    // no row of the warp sees this piece: P = 0 throughout
-#pragma unroll
-                                    for (int c = 0; c < 16; ++c) pk[c] = rk[c] = 0u;
-                                } else if (resid) {
-                                    masked(std::true_type{});
-                                } else {
-                                    masked(std::false_type{});
-                                }
-                                tmem_st_x16_nowait(s_addr + (uint32_t)(c0 + 16 * sc), pk);
-                                if (resid) {
                                     if (sc == 0) {
 #pragma unroll
                                         for (int c = 0; c < 16; ++c) rk0[c] = rk[c];
@@ -985,9 +987,9 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                     }
                                 }
                             }
-                            tmem_wait_st();
-                            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
                         }
+                        tmem_wait_st();
+                        l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
                     }
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(5, g);
                     if (lane == 0) CPA_TRACE_EVENT(44 + warp - C::kSmWarp0, g);
