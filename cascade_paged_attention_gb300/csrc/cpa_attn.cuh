@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             mbar_init(&ctrl->q_full[i], C::kQInTmem ? 128 : 1);
             mbar_init(&ctrl->q_empty[i], 1);
             mbar_init(&ctrl->s_full[i], 1);
-            mbar_init(&ctrl->p_full[i], 256);
+            mbar_init(&ctrl->p_full[i], 128 * C::kSplit);  // the warpgroups writing that P
             mbar_init(&ctrl->p_empty[i], 1);
         }
         mbar_init(&ctrl->o_full, 1);
@@ -642,9 +642,14 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             }
         } else if (warp == 1) {
             // ============================== MMA issuer
-            // Two cursors walk the same tile sequence: one issues S = Q K^T as soon
-            // as a tile's K/V and Q are in place, the other O += P V as soon as the
-            // softmax has written that tile's P.  Whichever is ready goes first.
+            // The work is a sequence of items, one per (tile, M tile): item i uses S
+            // buffer i % 2 (one M tile: consecutive tiles alternate between two S
+            // buffers; two M tiles: each M tile has its own).  Two cursors walk the
+            // items: one issues S = Q K^T as soon as an item's K/V and Q are in place
+            // and its S buffer is free (PV of item i - 2 issued), the other O += P V
+            // as soon as the softmax has written that item's P.  Whichever is ready
+            // goes first, so with two M tiles the tensor core works on one M tile
+            // while the softmax works on the other.
             if (lane == 0) {
                 const uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
                 const uint32_t idesc_o = idesc_bf16_f32(128, 128, true);
@@ -652,86 +657,86 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 TileCursor cs, cp;
                 cs.init(ctrl, p);
                 cp.init(ctrl, p);
-                long long gs = 0, gp = 0;  // next tile for S / for PV
-                const long long n_tiles = ctrl->count;
+                long long is = 0, ip = 0;  // next item for S / for PV
+                const long long n_items = ctrl->count * NUM_MT;
                 uint64_t t_idle = 0;
                 uint32_t spins = 0;
                 bool ok = true;
-                while (gp < n_tiles) {
+                while (ip < n_items) {
                     bool progressed = false;
-                    // S of tile gs overwrites the buffer that PV of tile gs - kSBufs reads
-                    if (gs < n_tiles && gs <= gp + C::kSBufs - 1) {
+                    if (is < n_items && is <= ip + 1) {
+                        const long long gs = is / NUM_MT;
+                        const int mt = (int)(is % NUM_MT);
                         const int qb = cs.w.seg % p.n_qbufs;
                         const int st = (int)(gs % p.n_stages);
                         const bool q_ready =
                             !cs.first() || mbar_test(&ctrl->q_full[qb], (cs.w.seg / p.n_qbufs) & 1);
                         if (q_ready &&
                             mbar_test(&ctrl->kv_full[st], (uint32_t)((gs / p.n_stages) & 1))) {
-                            CPA_TRACE_EVENT(2, gs);
+                            if (mt == 0) CPA_TRACE_EVENT(2, gs);
                             tc_fence_after_sync();
-                            const int sb = (int)(gs % C::kSBufs);
+                            const int sb = (int)(is & 1);
                             const uint32_t kb = sbase + p.off_kv + st * kStageBytes;
-                            for (int mt = 0; mt < NUM_MT; ++mt) {
-                                const uint32_t qa = sbase + p.off_q + (qb * NUM_MT + mt) * qmt_bytes;
+                            const uint32_t qa = sbase + p.off_q + (qb * NUM_MT + mt) * qmt_bytes;
+                            const uint32_t sd = tmem + C::s_col(0, 0) + (uint32_t)sb * 128u;
 #pragma unroll
-                                for (int kk = 0; kk < 8; ++kk) {
-                                    const uint64_t bd = sdesc_sw128(
-                                        kb + (kk >> 2) * kBN * 128 + (kk & 3) * 32, 16, 1024);
-                                    if (C::kQInTmem) {
-                                        umma_bf16_ts(tmem + C::s_col(mt, sb),
-                                                     tmem + C::q_col(qb) + kk * 8, bd, idesc_s,
-                                                     kk > 0 ? 1u : 0u);
-                                    } else {
-                                        const uint64_t ad = sdesc_sw128(
-                                            qa + (kk >> 2) * p.Rq * 128 + (kk & 3) * 32, 16, 1024);
-                                        umma_bf16_ss(tmem + C::s_col(mt, sb), ad, bd, idesc_s,
-                                                     kk > 0 ? 1u : 0u);
-                                    }
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t bd =
+                                    sdesc_sw128(kb + (kk >> 2) * kBN * 128 + (kk & 3) * 32, 16, 1024);
+                                if (C::kQInTmem) {
+                                    umma_bf16_ts(sd, tmem + C::q_col(qb) + kk * 8, bd, idesc_s,
+                                                 kk > 0 ? 1u : 0u);
+                                } else {
+                                    const uint64_t ad = sdesc_sw128(
+                                        qa + (kk >> 2) * p.Rq * 128 + (kk & 3) * 32, 16, 1024);
+                                    umma_bf16_ss(sd, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
                                 }
                             }
                             umma_commit(&ctrl->s_full[sb]);
-                            if (cs.last()) umma_commit(&ctrl->q_empty[qb]);
-                            CPA_TRACE_EVENT(15, gs);
-                            cs.advance(p);
-                            ++gs;
+                            if (mt == NUM_MT - 1) {
+                                if (cs.last()) umma_commit(&ctrl->q_empty[qb]);
+                                CPA_TRACE_EVENT(15, gs);
+                                cs.advance(p);
+                            }
+                            ++is;
                             progressed = true;
                         }
                     }
-                    if (gp < gs) {
-                        bool ready = mbar_test(&ctrl->p_full[gp % C::kSBufs],
-                                               (uint32_t)((gp / C::kSBufs) & 1));
+                    if (ip < is) {
+                        const long long gp = ip / NUM_MT;
+                        const int mt = (int)(ip % NUM_MT);
+                        const int sb = (int)(ip & 1);
+                        bool ready = mbar_test(&ctrl->p_full[sb], (uint32_t)((ip >> 1) & 1));
                         if (ready && cp.first() && cp.w.seg >= 1)
                             ready = mbar_test(&ctrl->o_empty, (uint32_t)((cp.w.seg - 1) & 1));
                         if (ready) {
-                            CPA_TRACE_EVENT(3, gp);
+                            if (mt == 0) CPA_TRACE_EVENT(3, gp);
                             tc_fence_after_sync();
                             const int st = (int)(gp % p.n_stages);
                             const uint32_t vb = sbase + p.off_kv + st * kStageBytes + 2 * kBN * 128;
                             const bool first = cp.first();
                             const int passes = cp.jj == cp.x.resid_tile ? 2 : 1;
-                            for (int mt = 0; mt < NUM_MT; ++mt) {
-                                // P of keys 64c..64c+63 (bf16, two per column) sits in the
-                                // first 32 of the 64 S columns those keys came from, its
-                                // residual in the other 32
-                                const uint32_t pa = tmem + C::s_col(mt, (int)(gp % C::kSBufs));
-                                for (int pass = 0; pass < passes; ++pass) {
+                            // P of keys 64c..64c+63 (bf16, two per column) sits in the
+                            // first 32 of the 64 S columns those keys came from, its
+                            // residual in the other 32
+                            const uint32_t pa = tmem + C::s_col(0, 0) + (uint32_t)sb * 128u;
+                            for (int pass = 0; pass < passes; ++pass) {
 #pragma unroll
-                                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                                        const uint64_t bd =
-                                            sdesc_sw128(vb + kk * 16 * 128, kBN * 128, 1024);
-                                        umma_bf16_ts(tmem + C::o_col(mt),
-                                                     pa + (kk >> 2) * 64 + pass * 32 + (kk & 3) * 8,
-                                                     bd, idesc_o,
-                                                     (first && pass == 0 && kk == 0) ? 0u : 1u);
-                                    }
+                                for (int kk = 0; kk < kBN / 16; ++kk) {
+                                    const uint64_t bd = sdesc_sw128(vb + kk * 16 * 128, kBN * 128, 1024);
+                                    umma_bf16_ts(tmem + C::o_col(mt),
+                                                 pa + (kk >> 2) * 64 + pass * 32 + (kk & 3) * 8, bd,
+                                                 idesc_o, (first && pass == 0 && kk == 0) ? 0u : 1u);
                                 }
                             }
-                            umma_commit(&ctrl->p_empty[gp % C::kSBufs]);
-                            umma_commit(&ctrl->kv_empty[st]);
-                            if (cp.last()) umma_commit(&ctrl->o_full);
-                            CPA_TRACE_EVENT(14, gp);
-                            cp.advance(p);
-                            ++gp;
+                            umma_commit(&ctrl->p_empty[sb]);
+                            if (mt == NUM_MT - 1) {
+                                umma_commit(&ctrl->kv_empty[st]);
+                                if (cp.last()) umma_commit(&ctrl->o_full);
+                                CPA_TRACE_EVENT(14, gp);
+                                cp.advance(p);
+                            }
+                            ++ip;
                             progressed = true;
                         }
                     }
@@ -742,12 +747,11 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         // (it frees a K/V stage), or on the next K/V tile when no PV is
                         // pending.  The thread wakes when the phase completes; the hint
                         // bounds the wait so the other barrier is re-checked.
-                        if (gp < gs)
-                            mbar_try_wait_hint(&ctrl->p_full[gp % C::kSBufs],
-                                               (uint32_t)((gp / C::kSBufs) & 1), 200);
-                        else if (gs < n_tiles)
-                            mbar_try_wait_hint(&ctrl->kv_full[(int)(gs % p.n_stages)],
-                                               (uint32_t)((gs / p.n_stages) & 1), 200);
+                        if (ip < is)
+                            mbar_try_wait_hint(&ctrl->p_full[ip & 1], (uint32_t)((ip >> 1) & 1), 200);
+                        else if (is < n_items)
+                            mbar_try_wait_hint(&ctrl->kv_full[(int)((is / NUM_MT) % p.n_stages)],
+                                               (uint32_t)(((is / NUM_MT) / p.n_stages) & 1), 200);
                     }
                     if (!progressed && (++spins & 63u) == 0) {
                         // same time limit as every other wait of the kernel
@@ -801,9 +805,11 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 float m_used = neg_inf(), l = 0.f;
                 const bool warp_inert = __all_sync(0xffffffffu, it >= x.ntok);
                 for (int jj = jb; jj < je; ++jj, ++g) {
+                    // this warpgroup's item: S buffer g % 2 (one M tile) or mt (two)
                     const int sb = (int)(g % C::kSBufs);
-                    bool okl = mbar_wait_warp(&ctrl->s_full[sb], (uint32_t)((g / C::kSBufs) & 1),
-                                              abort_flag, p.status);
+                    const int bi = C::kSBufs == 2 ? sb : mt;
+                    const uint32_t par = (uint32_t)((C::kSBufs == 2 ? g >> 1 : g) & 1);
+                    bool okl = mbar_wait_warp(&ctrl->s_full[bi], par, abort_flag, p.status);
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(4, g);
                     if (lane == 0) CPA_TRACE_EVENT(20 + warp - C::kSmWarp0, g);
                     const bool dtile = jj >= x.n_prefix;
@@ -883,10 +889,10 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         if (__any_sync(0xffffffffu, need)) {
                             // O holds PV of tiles up to g-1 of this unit: wait for it, then
                             // scale this thread's columns of O for rows whose max jumped
-                            const int pb = (int)((g - 1) % C::kSBufs);
-                            if (!mbar_wait_warp(&ctrl->p_empty[pb],
-                                                (uint32_t)(((g - 1) / C::kSBufs) & 1), abort_flag,
-                                                p.status)) {
+                            const int pb = C::kSBufs == 2 ? (int)((g - 1) & 1) : mt;
+                            const uint32_t ppar =
+                                (uint32_t)((C::kSBufs == 2 ? (g - 1) >> 1 : g - 1) & 1);
+                            if (!mbar_wait_warp(&ctrl->p_empty[pb], ppar, abort_flag, p.status)) {
                                 ok = false;  // the next barrier vote carries it to all threads
                             } else {
                                 tc_fence_after_sync();
@@ -1011,7 +1017,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     }
                     if (zeroed) fence_proxy_async_smem();  // the MMA reads those V rows
                     tc_fence_before_sync();
-                    mbar_arrive(&ctrl->p_full[sb]);
+                    mbar_arrive(&ctrl->p_full[bi]);
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(6, g);
                     if (lane == 0 && wgi == 0) CPA_TRACE_EVENT(9 + quarter, g);
                 }
