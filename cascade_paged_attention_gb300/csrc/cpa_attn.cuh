@@ -466,15 +466,17 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             mbar_init(&ctrl->kv_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&ctrl->q_full[i], C::kQInTmem ? 128 : 1);
+            mbar_init(&ctrl->q_full[i], C::kQInTmem ? 4 : 1);  // 4 epilogue warps / the TMA
             mbar_init(&ctrl->q_empty[i], 1);
             mbar_init(&ctrl->s_full[i], 1);
-            mbar_init(&ctrl->p_full[i], 128 * C::kSplit);  // the warpgroups writing that P
+            mbar_init(&ctrl->p_full[i], 4 * C::kSplit);  // the warps writing that P
             mbar_init(&ctrl->p_empty[i], 1);
         }
         mbar_init(&ctrl->o_full, 1);
-        mbar_init(&ctrl->o_empty, 128);
-        mbar_init(&ctrl->stats_full, 128 * NUM_MT);
+        // one arrival per warp (after __syncwarp): arrivals of every thread would
+        // serialise on the barrier's word
+        mbar_init(&ctrl->o_empty, 4);
+        mbar_init(&ctrl->stats_full, 4 * NUM_MT);
         mbar_init(&ctrl->mma_done, 1);
         mbar_init(&ctrl->merge_full, 1);
         ctrl->abort_flag = 0;
@@ -1017,7 +1019,8 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     }
                     if (zeroed) fence_proxy_async_smem();  // the MMA reads those V rows
                     tc_fence_before_sync();
-                    mbar_arrive(&ctrl->p_full[bi]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctrl->p_full[bi]);
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(6, g);
                     if (lane == 0 && wgi == 0) CPA_TRACE_EVENT(9 + quarter, g);
                 }
@@ -1035,7 +1038,8 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     }
                     if (ok) {
                         stats[R] = make_float2(m_used, l);
-                        mbar_arrive(&ctrl->stats_full);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ctrl->stats_full);
                     }
                 }
                 if (C::kSplit == 2) ok = bar_and(3, 256, ok);  // xsum and stats reuse
@@ -1078,7 +1082,8 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 __syncwarp();
                 tmem_st_x64(tmem + lane_addr + C::q_col(qb), v);
                 tc_fence_before_sync();
-                mbar_arrive(&ctrl->q_full[qb]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctrl->q_full[qb]);
             };
             Walker wq;  // runs two units ahead of `w` to stage Q
             wq.init(ctrl);
@@ -1155,7 +1160,8 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         });
                     }
                     tc_fence_before_sync();
-                    mbar_arrive(&ctrl->o_empty);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctrl->o_empty);
                 } else {
                     // A unit split over CTAs c_first..c_last: the piece that finishes last
                     // merges all pieces, in CTA order, so the result does not depend on
@@ -1213,7 +1219,8 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         }
                         if (et == 0) CPA_TRACE_EVENT(52, w.seg);
                         tc_fence_before_sync();
-                        mbar_arrive(&ctrl->o_empty);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ctrl->o_empty);
                         __threadfence();
                         named_bar_sync(1, 128);
                         if (et == 0) CPA_TRACE_EVENT(53, w.seg);
@@ -1343,7 +1350,8 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         }
                         if (mode == 2) {
                             tc_fence_before_sync();
-                            mbar_arrive(&ctrl->o_empty);
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&ctrl->o_empty);
                         }
                     }
                 }
