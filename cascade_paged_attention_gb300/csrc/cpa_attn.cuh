@@ -60,8 +60,8 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 static __device__ unsigned long long* cpa_trace_buf = nullptr;
 #define CPA_TRACE_EVENT(ev, idx)                                                  \
     do {                                                                          \
-        if (cpa_trace_buf && blockIdx.x < 4 && (idx) < 1024)                      \
-            cpa_trace_buf[(blockIdx.x * 64 + (ev)) * 1024 + (idx)] = clock64();   \
+        if (cpa_trace_local && blockIdx.x < 4 && (idx) < 1024)                    \
+            cpa_trace_local[(blockIdx.x * 64 + (ev)) * 1024 + (idx)] = clock64(); \
     } while (0)
 #else
 #define CPA_TRACE_EVENT(ev, idx) \
@@ -449,6 +449,9 @@ template <int NUM_MT>
 __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     paged_attn_kernel(const __grid_constant__ AttnParams p) {
     using C = Cfg<NUM_MT>;
+#ifdef CPA_TRACE
+    unsigned long long* const cpa_trace_local = cpa_trace_buf;  // read once
+#endif
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -503,9 +506,9 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     tc_fence_after_sync();
     schedule(p, ctrl);
 #ifdef CPA_TRACE
-    if (threadIdx.x == 0 && cpa_trace_buf && blockIdx.x < 4) {
-        cpa_trace_buf[(blockIdx.x * 64 + 13) * 1024 + 1000] = clock64();
-        cpa_trace_buf[(blockIdx.x * 64 + 13) * 1024 + 1001] = globaltimer_ns();
+    if (threadIdx.x == 0 && cpa_trace_local && blockIdx.x < 4) {
+        cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1000] = clock64();
+        cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1001] = globaltimer_ns();
     }
 #endif
     const uint32_t tmem = ctrl->tmem_base;
@@ -524,6 +527,8 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             Walker w;
             w.init(ctrl);
             long long g = 0;
+            int pst = 0;          // stage of tile g
+            uint32_t pkpar = 0;   // parity of that stage's current use
             bool ok = true;
             while (w.left > 0 && ok) {
                 const Unit x = get_unit(p, w.u);
@@ -560,12 +565,16 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 if (p.has_draft && je == x.n_tiles && lane < p.nbr)
                     dpage = __ldg(p.dtab + (size_t)(x.b * p.topk + x.branch0 + lane) * p.dtab_stride);
                 for (int jj = jb; jj < je; ++jj, ++g) {
-                    const int st = (int)(g % p.n_stages);
+                    // stage st of the ring, used for the (k+1)-th time; its previous use
+                    // had parity kpar ^ 1 (kept incrementally: no 64-bit division here)
+                    const int st = pst;
                     if (g >= p.n_stages) {
-                        ok = mbar_wait_warp(&ctrl->kv_empty[st],
-                                            (uint32_t)(((g / p.n_stages) - 1) & 1), abort_flag,
-                                            p.status);
+                        ok = mbar_wait_warp(&ctrl->kv_empty[st], pkpar ^ 1u, abort_flag, p.status);
                         if (!ok) break;
+                    }
+                    if (++pst == p.n_stages) {
+                        pst = 0;
+                        pkpar ^= 1u;
                     }
                     if (lane == 0) CPA_TRACE_EVENT(0, g);
                     uint8_t* stage = smem + p.off_kv + st * kStageBytes;
@@ -627,7 +636,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                             const int posi = key_base + (box0 + bi) * p.boxr;
                             tma_load_3d(stage + part * (kBN * 128) + bi * p.boxr * 128,
                                         part < 2 ? &p.kmap : &p.vmap, (part & 1) * 64, x.h,
-                                        pgi * p.P + (posi % p.P), &ctrl->kv_full[st], pol_kv);
+                                        pgi * p.P + (posi & (p.P - 1)), &ctrl->kv_full[st], pol_kv);
                         }
                     }
                 }
@@ -661,6 +670,10 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 cp.init(ctrl, p);
                 long long is = 0, ip = 0;  // next item for S / for PV
                 const long long n_items = ctrl->count * NUM_MT;
+                // K/V stage and kv_full parity of the tile S is at, and the stage of the
+                // tile PV is at, kept incrementally (no 64-bit division in this loop)
+                int st_s = 0, st_p = 0;
+                uint32_t par_s = 0;
                 uint64_t t_idle = 0;
                 uint32_t spins = 0;
                 bool ok = true;
@@ -669,12 +682,12 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     if (is < n_items && is <= ip + 1) {
                         const long long gs = is / NUM_MT;
                         const int mt = (int)(is % NUM_MT);
-                        const int qb = cs.w.seg % p.n_qbufs;
-                        const int st = (int)(gs % p.n_stages);
-                        const bool q_ready =
-                            !cs.first() || mbar_test(&ctrl->q_full[qb], (cs.w.seg / p.n_qbufs) & 1);
-                        if (q_ready &&
-                            mbar_test(&ctrl->kv_full[st], (uint32_t)((gs / p.n_stages) & 1))) {
+                        const int qb = p.n_qbufs == 2 ? (cs.w.seg & 1) : 0;
+                        const uint32_t qpar =
+                            (uint32_t)((p.n_qbufs == 2 ? cs.w.seg >> 1 : cs.w.seg) & 1);
+                        const int st = st_s;
+                        const bool q_ready = !cs.first() || mbar_test(&ctrl->q_full[qb], qpar);
+                        if (q_ready && mbar_test(&ctrl->kv_full[st], par_s)) {
                             if (mt == 0) CPA_TRACE_EVENT(2, gs);
                             tc_fence_after_sync();
                             const int sb = (int)(is & 1);
@@ -699,6 +712,10 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                 if (cs.last()) umma_commit(&ctrl->q_empty[qb]);
                                 CPA_TRACE_EVENT(15, gs);
                                 cs.advance(p);
+                                if (++st_s == p.n_stages) {
+                                    st_s = 0;
+                                    par_s ^= 1u;
+                                }
                             }
                             ++is;
                             progressed = true;
@@ -714,7 +731,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         if (ready) {
                             if (mt == 0) CPA_TRACE_EVENT(3, gp);
                             tc_fence_after_sync();
-                            const int st = (int)(gp % p.n_stages);
+                            const int st = st_p;
                             const uint32_t vb = sbase + p.off_kv + st * kStageBytes + 2 * kBN * 128;
                             const bool first = cp.first();
                             const int passes = cp.jj == cp.x.resid_tile ? 2 : 1;
@@ -737,6 +754,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                 if (cp.last()) umma_commit(&ctrl->o_full);
                                 CPA_TRACE_EVENT(14, gp);
                                 cp.advance(p);
+                                if (++st_p == p.n_stages) st_p = 0;
                             }
                             ++ip;
                             progressed = true;
@@ -752,8 +770,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         if (ip < is)
                             mbar_try_wait_hint(&ctrl->p_full[ip & 1], (uint32_t)((ip >> 1) & 1), 200);
                         else if (is < n_items)
-                            mbar_try_wait_hint(&ctrl->kv_full[(int)((is / NUM_MT) % p.n_stages)],
-                                               (uint32_t)(((is / NUM_MT) / p.n_stages) & 1), 200);
+                            mbar_try_wait_hint(&ctrl->kv_full[st_s], par_s, 200);
                     }
                     if (!progressed && (++spins & 63u) == 0) {
                         // same time limit as every other wait of the kernel
@@ -1374,9 +1391,9 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
 #ifdef CPA_TRACE
-    if (threadIdx.x == 0 && cpa_trace_buf && blockIdx.x < 4) {
-        cpa_trace_buf[(blockIdx.x * 64 + 13) * 1024 + 1002] = clock64();
-        cpa_trace_buf[(blockIdx.x * 64 + 13) * 1024 + 1003] = globaltimer_ns();
+    if (threadIdx.x == 0 && cpa_trace_local && blockIdx.x < 4) {
+        cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1002] = clock64();
+        cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1003] = globaltimer_ns();
     }
 #endif
     if (warp == 1) {
