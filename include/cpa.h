@@ -119,7 +119,8 @@ size_t cpa_cascade_verify_workspace_size(int B, int topk, int S, int H_q, int H_
  *   lse                fp32 [B*topk*S, H_q] output (natural log).
  * Supported: head_dim 128; page_size in {8,16,32,64,128,256}; 1 <= S <= 16
  * and S <= page_size (a branch's drafts share its first draft page);
- * topk <= 8 when S <= 8, topk <= 4 when S > 8; topk*S*(H_q/H_kv) <= 256.
+ * topk <= 16 when S <= 8, topk <= 8 when S > 8 (the branches' draft blocks of
+ * 8 or 16 rows fill one 128-key tile); topk*S*(H_q/H_kv) <= 256.
  */
 cpa_status cpa_cascade_verify(const void* q, const void* k_pages, const void* v_pages,
                               const int32_t* prefix_page_table, int prefix_pt_stride,

@@ -34,6 +34,11 @@ SMALL_VERIFY = {
                        prefix_lens=[700, 1500], seed=34),
     "pages128": dict(B=2, topk=2, S=3, H_q=32, H_kv=8, page_size=128,
                      prefix_lens=[1000, 257], seed=35),
+    # the widest draft tiles: 16 branches of 8-row blocks, 8 branches of 16-row blocks
+    "topk16_s5": dict(B=2, topk=16, S=5, H_q=8, H_kv=8, page_size=16,
+                      prefix_lens=[200, 1000], seed=36),
+    "topk8_s12_two_mtiles": dict(B=2, topk=8, S=12, H_q=16, H_kv=8, page_size=16,
+                                 prefix_lens=[300, 40], seed=37),
 }
 
 
