@@ -137,6 +137,23 @@ def cpu_oracle_sample(wl, n_requests: int, threads: int = 0, min_seconds: float 
     return kv_bytes * passes / dt / 1e9, dt, passes
 
 
+def reduce_max(x: float, pg=None, device=None) -> float:
+    """The largest x over all ranks (x itself without a process group)."""
+    if pg is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_gbs(bytes_per_rank: float, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job GB/s: every rank moved bytes_per_rank per step; the job took the
+    slowest rank's time."""
+    return bytes_per_rank * world * steps / (total_ms * 1e-3) / 1e9
+
+
 def dist_init():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -153,7 +170,9 @@ def run_reference(args, world, rank):
     oracle.build.build()
     wl = cpa_synth.make_verify(**cpa_synth.VERIFY_CONFIGS[CFG])
     cores = os.cpu_count() or 1
-    n_req = 8  # one step: every row of 8 of the 64 requests (about 0.1 s on 16 cores)
+    # one step: every row of n_req of the 64 requests (about 16 ms each on 16 cores),
+    # sized so that the whole run stays within a couple of minutes for any --steps
+    n_req = max(1, min(wl.B, round(3000 / max(1, args.steps + args.warmup))))
     for _ in range(args.warmup):
         cpu_oracle_sample(wl, n_req)
     vals, times = [], []
@@ -237,11 +256,7 @@ def run_ours(args, world, rank, local):
             pg.barrier()
 
     def max_over_ranks(x: float) -> float:
-        if pg is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, pg, dev)
 
     def timed(fn, steps, per_launch=False):
         """Time `steps` calls: total ms (events around the whole run) and per-call ms."""
@@ -268,7 +283,7 @@ def run_ours(args, world, rank, local):
     clock_info = clocks.stop()
     total_ms = max_over_ranks(total_ms)
     ms_per_step = total_ms / args.steps
-    value = unique_bytes * world * args.steps / (total_ms * 1e-3) / 1e9
+    value = weak_scaling_gbs(unique_bytes, world, args.steps, total_ms)
     launch_ms = statistics.mean(per_ms)
     achieved = unique_bytes / (launch_ms * 1e-3) / 1e9
 
@@ -296,7 +311,7 @@ def run_ours(args, world, rank, local):
     e2e_steps = max(3, min(args.steps, 10))
     e2e_total, _ = timed(e2e_step, e2e_steps)
     e2e_total = max_over_ranks(e2e_total)
-    e2e_value = unique_bytes * world * e2e_steps / (e2e_total * 1e-3) / 1e9
+    e2e_value = weak_scaling_gbs(unique_bytes, world, e2e_steps, e2e_total)
 
     peak, peak_kind = measured_peaks()
     traffic = None
