@@ -233,6 +233,7 @@ struct Ctrl {
     int64_t ustart;  // global tile index where the first unit starts
     int n_ctas;      // CTAs that have work
     int u0, j0;      // first unit and its first tile
+    int rr, ppg, qtn;  // prefill: pairs dealt round-robin, pairs per group, q tiles per group
     int flag;
     int found;
     long long scan[32];
@@ -320,13 +321,41 @@ __device__ __forceinline__ void schedule(const AttnParams& p, Ctrl* c) {
             total += tot;
         }
     } else {
-        long long gt = 0;
-        for (int qt = 0; qt < p.QT; ++qt) gt += prefill_qt_tiles(p, qt);
-        total = gt * p.B * p.H_kv;
+        // Prefill: every q tile of a group (request, KV head) reads the same keys
+        // from the start, so the work is dealt so that the CTAs running at any one
+        // time work on the same groups and share each K/V tile through L2: the
+        // pairs (q tile j, q tile QT-1-j) of a group, which have equal tile sums,
+        // go round-robin over the CTAs in group order.  Units are never split.
+        if (threadIdx.x == 0) {
+            const int ppg = (p.QT + 1) / 2;
+            const long long pairs = (long long)p.B * p.H_kv * ppg;
+            const int n = (int)(pairs < (long long)gridDim.x ? pairs : (long long)gridDim.x);
+            const int cta = blockIdx.x;
+            c->rr = 1;
+            c->ppg = ppg;
+            c->qtn = p.QT;
+            c->n_ctas = n;
+            c->total = 0;
+            c->found = 1;
+            long long cnt = 0;
+            for (long long pid = cta; pid < pairs && cta < n; pid += n) {
+                const int jp = (int)(pid % ppg);
+                cnt += prefill_qt_tiles(p, jp);
+                if (p.QT - 1 - jp != jp) cnt += prefill_qt_tiles(p, p.QT - 1 - jp);
+            }
+            c->count = cnt;
+            c->begin = 0;
+            c->u0 = (int)((cta / ppg) * p.QT + cta % ppg);
+            c->j0 = 0;
+            c->ustart = cta;  // the pair this CTA starts with
+        }
+        __syncthreads();
+        return;
     }
     const int n_ctas = (int)(total < (long long)gridDim.x ? total : (long long)gridDim.x);
     const int cta = blockIdx.x;
     if (threadIdx.x == 0) {
+        c->rr = 0;
         c->total = total;
         c->n_ctas = n_ctas;
         c->found = 0;
@@ -364,22 +393,6 @@ __device__ __forceinline__ void schedule(const AttnParams& p, Ctrl* c) {
             __syncthreads();
             if (c->found) break;
         }
-    } else if (threadIdx.x == 0) {
-        long long gt = 0;
-        for (int qt = 0; qt < p.QT; ++qt) gt += prefill_qt_tiles(p, qt);
-        const long long grp = t0 / gt;
-        long long acc = grp * gt;
-        for (int qt = 0; qt < p.QT; ++qt) {
-            const int n = prefill_qt_tiles(p, qt);
-            if (t0 < acc + n) {
-                c->u0 = (int)(grp * p.QT + qt);
-                c->j0 = (int)(t0 - acc);
-                c->ustart = acc;
-                break;
-            }
-            acc += n;
-        }
-        c->found = 1;
     }
     __syncthreads();
 }
@@ -403,12 +416,24 @@ struct Walker {
         const long long rest = (long long)x.n_tiles - j;
         je = (int)(j + (left < rest ? left : rest));
     }
-    __device__ __forceinline__ void next(const Unit& x, int jb, int je) {
+    __device__ __forceinline__ void next(const Unit& x, int jb, int je, const Ctrl* c) {
         left -= (je - jb);
-        ustart += x.n_tiles;
-        ++u;
         j = 0;
         ++seg;
+        if (!c->rr) {
+            ustart += x.n_tiles;
+            ++u;
+            return;
+        }
+        // round-robin prefill: ustart is the current pair
+        const int QT = c->qtn, pid = (int)ustart, jp = pid % c->ppg;
+        if (u % QT == jp && QT - 1 - jp != jp) {
+            u += QT - 1 - 2 * jp;  // the pair's second q tile
+        } else {
+            const int nxt = pid + c->n_ctas;
+            ustart = nxt;
+            u = (nxt / c->ppg) * QT + nxt % c->ppg;
+        }
     }
 };
 
@@ -428,9 +453,9 @@ struct TileCursor {
     }
     __device__ __forceinline__ bool first() const { return jj == jb; }
     __device__ __forceinline__ bool last() const { return jj == je - 1; }
-    __device__ __forceinline__ void advance(const AttnParams& p) {
+    __device__ __forceinline__ void advance(const AttnParams& p, const Ctrl* c) {
         if (++jj == je) {
-            w.next(x, jb, je);
+            w.next(x, jb, je, c);
             if (w.left > 0) {
                 x = get_unit(p, w.u);
                 w.piece(x, jb, je);
@@ -519,7 +544,9 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     if (ctrl->count > 0) {
         if (warp == 0) {
             // ============================== producer
-            const uint64_t pol_kv = l2_policy_evict_first();
+            // verify reads each K/V tile once; prefill reads it once per q tile
+            const uint64_t pol_kv =
+                is_verify(p.mode) ? l2_policy_evict_first() : l2_policy_evict_normal();
             const uint64_t pol_q = l2_policy_evict_last();
             const int NB = kBN / p.boxr;
             const uint32_t q_tx = (uint32_t)(NUM_MT * 2 * G * p.TSB * 128);
@@ -640,7 +667,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         }
                     }
                 }
-                w.next(x, jb, je);
+                w.next(x, jb, je, ctrl);
             }
             // make sure no TMA write is still in flight when the CTA leaves
             const long long filled = g;
@@ -711,7 +738,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                             if (mt == NUM_MT - 1) {
                                 if (cs.last()) umma_commit(&ctrl->q_empty[qb]);
                                 CPA_TRACE_EVENT(15, gs);
-                                cs.advance(p);
+                                cs.advance(p, ctrl);
                                 if (++st_s == p.n_stages) {
                                     st_s = 0;
                                     par_s ^= 1u;
@@ -753,7 +780,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                 umma_commit(&ctrl->kv_empty[st]);
                                 if (cp.last()) umma_commit(&ctrl->o_full);
                                 CPA_TRACE_EVENT(14, gp);
-                                cp.advance(p);
+                                cp.advance(p, ctrl);
                                 if (++st_p == p.n_stages) st_p = 0;
                             }
                             ++ip;
@@ -1060,7 +1087,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     }
                 }
                 if (C::kSplit == 2) ok = bar_and(3, 256, ok);  // xsum and stats reuse
-                w.next(x, jb, je);
+                w.next(x, jb, je, ctrl);
             }
         } else if (warp >= C::kEpiWarp0) {
             // ============================== epilogue
@@ -1111,7 +1138,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     int qjb, qje;
                     wq.piece(xq, qjb, qje);
                     load_q(xq, q_loaded);
-                    wq.next(xq, qjb, qje);
+                    wq.next(xq, qjb, qje, ctrl);
                 }
             }
             Walker w;
@@ -1381,9 +1408,9 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     wq.piece(xq, qjb, qje);
                     load_q(xq, q_loaded % 2);
                     ++q_loaded;
-                    wq.next(xq, qjb, qje);
+                    wq.next(xq, qjb, qje, ctrl);
                 }
-                w.next(x, jb, je);
+                w.next(x, jb, je, ctrl);
             }
         }
     }
