@@ -36,6 +36,11 @@ __all__ = [
     "PrefillWorkload",
     "make_verify",
     "make_prefill",
+    "TreeWorkload",
+    "make_tree_verify",
+    "random_bfs_tree",
+    "chain_forest",
+    "TREE_CONFIGS",
     "VERIFY_CONFIGS",
     "PREFILL_CONFIG",
     "bf16_bits_from_f32",
@@ -271,6 +276,135 @@ def make_prefill(B: int, N: int, H: int, H_q: int, H_kv: int, head_dim: int = 12
     return wl
 
 
+def random_bfs_tree(rng: np.random.Generator, N: int, n_roots: int = 1,
+                    max_children: int = 4) -> np.ndarray:
+    """A random draft tree of N nodes, returned as a BFS-ordered parent array.
+
+    Nodes are produced level by level: the first ``n_roots`` nodes are roots
+    (parent -1); each later node picks its parent uniformly among the nodes of
+    the previous level that still have fewer than ``max_children`` children,
+    and a new level starts once a level's nodes are used up.  Because nodes
+    are numbered in creation order and parents are picked in ascending order,
+    the numbering is a BFS order (every parent precedes its children and the
+    children of an earlier node precede those of a later one).
+    """
+    assert 1 <= n_roots <= N
+    parents = [-1] * n_roots
+    level = list(range(n_roots))
+    while len(parents) < N:
+        n_next = int(rng.integers(1, max_children * len(level) + 1))
+        n_next = min(n_next, N - len(parents))
+        picks = sorted(int(x) for x in rng.choice(
+            np.repeat(np.array(level), max_children), size=n_next, replace=False))
+        start = len(parents)
+        parents.extend(picks)
+        level = list(range(start, len(parents)))
+    return np.asarray(parents, dtype=np.int32)
+
+
+def chain_forest(topk: int, S: int) -> np.ndarray:
+    """Parent array of topk independent chains of S drafts, in BFS order.
+
+    Level s holds draft s of every branch, so draft s of branch k is node
+    ``s*topk + k`` and its parent is node ``(s-1)*topk + k``.
+    """
+    par = np.full(topk * S, -1, dtype=np.int32)
+    for s in range(1, S):
+        for k in range(topk):
+            par[s * topk + k] = (s - 1) * topk + k
+    return par
+
+
+@dataclasses.dataclass
+class TreeWorkload:
+    """Inputs of one tree-verify step: B requests, each with a BFS-flattened draft tree of N nodes."""
+
+    B: int
+    N: int
+    H_q: int
+    H_kv: int
+    head_dim: int
+    page_size: int
+    prefix_lens: np.ndarray          # int32 [B]
+    parents: np.ndarray              # int32 [B, N], -1 for roots
+    q: np.ndarray                    # uint16 [B*N, H_q, d], token b*N + i
+    k_pages: np.ndarray
+    v_pages: np.ndarray
+    prefix_page_table: np.ndarray    # int32 [B, max_prefix_pages]
+    tree_page_table: np.ndarray      # int32 [B, ceil(N/P)]
+    max_prefix_len: int
+    prefix_k: Optional[list] = None  # logical K/V per request (optional)
+    prefix_v: Optional[list] = None
+    tree_k: Optional[list] = None
+    tree_v: Optional[list] = None
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_pages.shape[0])
+
+    @property
+    def n_tokens(self) -> int:
+        return self.B * self.N
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    def unique_kv_tokens(self) -> int:
+        return int(self.prefix_lens.astype(np.int64).sum()) + self.B * self.N
+
+    def kv_bytes_per_token(self) -> int:
+        return 2 * self.H_kv * self.head_dim * 2
+
+
+def make_tree_verify(B: int, N: int, H_q: int, H_kv: int, head_dim: int = 128,
+                     page_size: int = 16, L: Optional[int] = None,
+                     L_range: Optional[tuple[int, int]] = None, prefix_lens=None,
+                     parents=None, n_roots: int = 1, max_children: int = 4, seed: int = 0,
+                     perm_seed: Optional[int] = None, pad_fill: str = "random",
+                     keep_logical: bool = False) -> TreeWorkload:
+    """Build one tree-verify workload.
+
+    ``parents`` (int ``[N]`` shared by every request, or ``[B, N]``) fixes
+    the trees; otherwise each request draws its own ``random_bfs_tree``.
+    Logical contents depend only on ``seed``, page placement only on
+    ``perm_seed``.
+    """
+    rng = np.random.default_rng(seed)
+    if prefix_lens is not None:
+        lens = np.asarray(prefix_lens, dtype=np.int32).copy()
+        assert lens.shape == (B,)
+    elif L_range is not None:
+        lens = rng.integers(L_range[0], L_range[1] + 1, size=B).astype(np.int32)
+    else:
+        assert L is not None
+        lens = np.full(B, L, dtype=np.int32)
+    if parents is None:
+        par = np.stack([random_bfs_tree(rng, N, n_roots, max_children) for _ in range(B)])
+    else:
+        par = np.asarray(parents, dtype=np.int32)
+        par = np.broadcast_to(par, (B, N)).copy() if par.ndim == 1 else par.copy()
+    assert par.shape == (B, N)
+    P = page_size
+    d = head_dim
+    q = _normal_bf16(rng, (B * N, H_q, d))
+    pk = [_normal_bf16(rng, (int(lens[b]), H_kv, d)) for b in range(B)]
+    pv = [_normal_bf16(rng, (int(lens[b]), H_kv, d)) for b in range(B)]
+    tk = [_normal_bf16(rng, (N, H_kv, d)) for _ in range(B)]
+    tv = [_normal_bf16(rng, (N, H_kv, d)) for _ in range(B)]
+    perm_rng = np.random.default_rng(seed * 7919 + 17 if perm_seed is None else perm_seed)
+    k_pages, v_pages, tables = build_pool(pk + tk, pv + tv, P, perm_rng, pad_fill)
+    max_prefix_len = int(lens.max()) if B > 0 else 0
+    wl = TreeWorkload(B=B, N=N, H_q=H_q, H_kv=H_kv, head_dim=d, page_size=P, prefix_lens=lens,
+                      parents=par, q=q, k_pages=k_pages, v_pages=v_pages,
+                      prefix_page_table=table_matrix(tables[:B], (max_prefix_len + P - 1) // P),
+                      tree_page_table=table_matrix(tables[B:], (N + P - 1) // P),
+                      max_prefix_len=max_prefix_len)
+    if keep_logical:
+        wl.prefix_k, wl.prefix_v, wl.tree_k, wl.tree_v = pk, pv, tk, tv
+    return wl
+
+
 # The five workloads the method is exercised on, by name.  Verify shapes come
 # from the pages' example (L=2000, topk=4, S=5) and its neighbours.
 VERIFY_CONFIGS = {
@@ -279,5 +413,13 @@ VERIFY_CONFIGS = {
     "pages_example": dict(B=64, topk=4, S=5, L=2000, H_q=32, H_kv=8, page_size=16, seed=3),
     "long_variable": dict(B=16, topk=8, S=4, L_range=(1024, 32768), H_q=64, H_kv=8,
                           page_size=64, seed=4),
+}
+# Draft-tree verify: the pages' example request shape (L=2000, H_q=32,
+# H_kv=8) with one 20-node tree per request in place of 4 chains of 5, and a
+# 60-node tree, the size of an EAGLE-2-style dynamic tree.
+TREE_CONFIGS = {
+    "tree_tiny": dict(B=2, N=7, L=64, H_q=8, H_kv=2, page_size=16, seed=11),
+    "tree_pages_example": dict(B=64, N=20, L=2000, H_q=32, H_kv=8, page_size=16, seed=12),
+    "tree_60": dict(B=64, N=60, L=2000, H_q=32, H_kv=8, page_size=16, seed=13),
 }
 PREFILL_CONFIG = dict(B=8, N=8192, H_q=32, H_kv=8, page_size=16, seed=5, hits=(0.0, 0.5, 0.75))

@@ -14,6 +14,13 @@ What is computed, and from which passage:
   ("Topk > 1" section of the same page).  ``part="prefix"`` / ``"draft"``
   restrict the key set to the Pass A / Pass B piece of the same page's
   two-segment decomposition.
+* ``ancestor_masks``: the tree-attention mask of the KV-cache tutorial
+  (section 8.2 tip box; interview question Q14): tree nodes flattened in BFS
+  order, A(i) = the ancestors of node i with i itself, M[i, j] = 1 iff j is in
+  A(i).  Built bottom-up, A(i) = {i} plus A(parent(i)).
+* ``tree_verify``: verify over a general draft tree: node i of request b sees
+  the request's prefix and the nodes of A(i).  ``part="prefix"`` /
+  ``"draft"`` restrict it to the prefix / the tree nodes, as for ``verify``.
 * ``prefill``: suffix query i of a prefix-hit prefill sees keys 0..H+i
   (rectangle 0..H-1 plus triangle H..H+i), "Causal Attention ... KV hit area"
   page, sections 1-2.
@@ -56,6 +63,9 @@ def _load():
         lib.oracle_prefill.restype = i32
         lib.oracle_prefill.argtypes = [P, P, P, i64, P, i32, i32, i32, i32, i32, i32, i32, i32,
                                        i32, f64, P, i64, P, P, i32]
+        lib.oracle_tree_verify.restype = i32
+        lib.oracle_tree_verify.argtypes = [P, P, P, i64, P, i32, P, i32, P, P, i32, i32, i32,
+                                           i32, i32, i32, i32, f64, P, i64, P, P, i32]
         lib.oracle_merge_state.restype = None
         lib.oracle_merge_state.argtypes = [P, P, P, P, i64, i32, P, P]
         _lib = lib
@@ -114,6 +124,80 @@ def verify_wl(wl, part: str = "full", rows=None, threads: int = 0):
     return verify(wl.q, wl.k_pages, wl.v_pages, wl.prefix_page_table, wl.draft_page_table,
                   wl.prefix_lens, wl.topk, wl.S, wl.H_q, wl.H_kv, part=part, rows=rows,
                   threads=threads)
+
+
+def ancestor_masks(parents) -> np.ndarray:
+    """Ancestor-or-self bitmasks of BFS-flattened draft trees.
+
+    ``parents`` is int ``[N]`` or ``[B, N]``: ``parents[i]`` is the BFS index
+    of node i's parent, or -1 for a root (a node whose parent is the last
+    prefix token).  BFS flattening lists every parent before its children, so
+    ``parents[i] < i`` is required.  Returns uint64 of the same shape whose
+    bit j is M[i, j]: 1 when j is i or an ancestor of i (KV-cache tutorial,
+    section 8.2 tip box and Q14).  N <= 64.
+    """
+    par = np.asarray(parents, dtype=np.int64)
+    flat = par.reshape(-1, par.shape[-1])
+    N = flat.shape[1]
+    if N < 1 or N > 64:
+        raise ValueError("a tree has 1..64 nodes")
+    out = np.zeros(flat.shape, dtype=np.uint64)
+    for r in range(flat.shape[0]):
+        for i in range(N):
+            pi = int(flat[r, i])
+            if pi < -1 or pi >= i:
+                raise ValueError(f"parent of node {i} is {pi}: not a BFS-flattened tree")
+            # A(i) = {i} together with A(parent(i)); the parent's set is already built
+            mask = 1 << i
+            if pi >= 0:
+                mask |= int(out[r, pi])
+            out[r, i] = np.uint64(mask)
+    return out.reshape(par.shape)
+
+
+def tree_verify(q, k_pages, v_pages, prefix_page_table, tree_page_table, prefix_lens, parents,
+                H_q: int, H_kv: int, scale: Optional[float] = None, part: str = "full",
+                rows: Optional[Sequence[int]] = None, threads: int = 0):
+    """fp64 verify attention over general draft trees.
+
+    ``parents`` int ``[B, N]`` (BFS order, see ``ancestor_masks``); ``q`` is
+    ``[B*N, H_q, d]`` with token ``b*N + i`` node i of request b; tree node j
+    of request b sits at logical position j of ``tree_page_table[b]``.  Rows
+    are ``token * H_q + head``.  Returns (o [n_rows, d], lse [n_rows]).
+    """
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    kp = np.ascontiguousarray(k_pages, dtype=np.uint16)
+    vp = np.ascontiguousarray(v_pages, dtype=np.uint16)
+    ppt = np.ascontiguousarray(prefix_page_table, dtype=np.int32)
+    tpt = np.ascontiguousarray(tree_page_table, dtype=np.int32)
+    lens = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+    par = np.asarray(parents)
+    B = int(lens.shape[0])
+    N = int(par.shape[-1])
+    masks = np.ascontiguousarray(ancestor_masks(par.reshape(B, N)).reshape(-1))
+    d = int(q.shape[-1])
+    P = int(kp.shape[1])
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    r, rp, nr = _rows_arg(rows)
+    n = nr if r is not None else B * N * H_q
+    o = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    err = lib.oracle_tree_verify(_ptr(q), _ptr(kp), _ptr(vp), int(kp.shape[0]), _ptr(ppt),
+                                 int(ppt.shape[1]), _ptr(tpt), int(tpt.shape[1]), _ptr(lens),
+                                 _ptr(masks), B, N, H_q, H_kv, d, P, PART_CODES[part],
+                                 float(scale), rp, nr, _ptr(o), _ptr(lse), threads)
+    if err:
+        raise ValueError(f"oracle_tree_verify: {_ERR.get(err, err)}")
+    return o, lse
+
+
+def tree_verify_wl(wl, part: str = "full", rows=None, threads: int = 0):
+    """``tree_verify`` on a ``cpa_synth.TreeWorkload``-shaped object."""
+    return tree_verify(wl.q, wl.k_pages, wl.v_pages, wl.prefix_page_table, wl.tree_page_table,
+                       wl.prefix_lens, wl.parents, wl.H_q, wl.H_kv, part=part, rows=rows,
+                       threads=threads)
 
 
 def prefill(q, k_pages, v_pages, page_table, B: int, N: int, H: int, H_q: int, H_kv: int,

@@ -22,6 +22,13 @@
  *     own branch's drafts 0..s (its ancestors, itself included -- the tree
  *     attention mask of the KV-cache tutorial, Q14, puts each node in its own
  *     ancestor set).  Pass A is the prefix part alone, Pass B the draft part.
+ *   - tree verify (KV-cache tutorial, section 8.2 tip box on tree attention,
+ *     and interview question Q14): the draft tokens of request b are the N
+ *     nodes of a token tree flattened in BFS order; node i sees the whole
+ *     prefix and the tree nodes j with M[i, j] = 1, M being the ancestor mask
+ *     (j is i or an ancestor of i).  The mask arrives as one 64-bit row per
+ *     node, bit j = M[i, j]; the chain-per-branch case above is the forest of
+ *     topk chains.
  *   - prefix-hit prefill ("Causal Attention: why attention scales by 1-h^2
  *     after a KV hit", sections 1-2): suffix query i, at absolute position
  *     H+i, sees keys 0..H+i (the rectangle 0..H-1 plus the triangle H..H+i);
@@ -98,7 +105,7 @@ static void attend_one(const double *q, const uint16_t *k_pages, const uint16_t 
 /* Problem descriptions                                                */
 /* ------------------------------------------------------------------ */
 
-enum { KIND_VERIFY = 0, KIND_PREFILL = 1 };
+enum { KIND_VERIFY = 0, KIND_PREFILL = 1, KIND_TREE = 2 };
 /* part: 0 = full visible set, 1 = first piece only (prefix / rectangle),
  *       2 = second piece only (own drafts / causal triangle).            */
 
@@ -112,6 +119,10 @@ typedef struct {
     /* verify */
     const int32_t *prefix_pt, *draft_pt, *prefix_lens;
     int prefix_stride, draft_stride, B, topk, S;
+    /* tree verify (also uses prefix_pt, prefix_stride, prefix_lens, B, N) */
+    const int32_t *tree_pt;
+    int tree_stride;
+    const uint64_t *masks;
     /* prefill */
     const int32_t *pt;
     int pt_stride, N, H;
@@ -153,6 +164,19 @@ static int visible_keys(const problem_t *p, int64_t token, int head, int64_t *ke
         if (p->part != 1) {
             const int32_t *row = p->draft_pt + ((int64_t)b * p->topk + branch) * p->draft_stride;
             for (int j = 0; j <= s; ++j) key_off[n++] = key_offset(p, row, j, kv_head, &bad);
+        }
+    } else if (p->kind == KIND_TREE) {
+        int b = (int)(token / p->N);
+        if (p->part != 2) {
+            const int32_t *row = p->prefix_pt + (int64_t)b * p->prefix_stride;
+            int L = p->prefix_lens[b];
+            for (int pos = 0; pos < L; ++pos) key_off[n++] = key_offset(p, row, pos, kv_head, &bad);
+        }
+        if (p->part != 1) {
+            const int32_t *row = p->tree_pt + (int64_t)b * p->tree_stride;
+            uint64_t m = p->masks[token];
+            for (int j = 0; j < p->N; ++j)
+                if ((m >> j) & 1u) key_off[n++] = key_offset(p, row, j, kv_head, &bad);
         }
     } else {
         int M = p->N - p->H;
@@ -261,6 +285,49 @@ int oracle_verify(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_
         for (int64_t r = 0; r < n_rows; ++r)
             if (rows[r] < 0 || rows[r] >= total_rows) return ORACLE_BAD_ARG;
     p.max_keys = maxL + S;
+    p.o = o; p.lse = lse;
+    return run_rows(&p, n_threads);
+}
+
+/*
+ * Tree verify for rows (token, head), token = b * N + i the BFS index i of
+ * a node of request b's draft tree.  masks[token] bit j set means node i sees
+ * tree node j (stored at logical position j of tree_pt row b).  part 0 =
+ * prefix + masked tree nodes, 1 = prefix only, 2 = tree nodes only.
+ * 1 <= N <= 64; bits at or above N must be clear.
+ */
+int oracle_tree_verify(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                       int64_t num_pages, const int32_t *prefix_pt, int prefix_stride,
+                       const int32_t *tree_pt, int tree_stride, const int32_t *prefix_lens,
+                       const uint64_t *masks, int B, int N, int H_q, int H_kv, int d, int P,
+                       int part, double scale, const int64_t *rows, int64_t n_rows, double *o,
+                       double *lse, int n_threads) {
+    if (B < 0 || N < 1 || N > 64 || H_kv < 1 || H_q % H_kv != 0 || d < 1 || P < 1 || part < 0 ||
+        part > 2)
+        return ORACLE_BAD_ARG;
+    problem_t p;
+    memset(&p, 0, sizeof p);
+    p.kind = KIND_TREE;
+    p.part = part;
+    p.q = q; p.k_pages = k_pages; p.v_pages = v_pages; p.num_pages = num_pages;
+    p.H_q = H_q; p.H_kv = H_kv; p.d = d; p.P = P; p.scale = scale;
+    p.prefix_pt = prefix_pt; p.prefix_stride = prefix_stride; p.prefix_lens = prefix_lens;
+    p.tree_pt = tree_pt; p.tree_stride = tree_stride; p.masks = masks;
+    p.B = B; p.N = N;
+    int64_t total_rows = (int64_t)B * N * H_q;
+    p.rows = rows;
+    p.n_rows = rows ? n_rows : total_rows;
+    int maxL = 0;
+    for (int b = 0; b < B; ++b) {
+        if (prefix_lens[b] < 0) return ORACLE_BAD_ARG;
+        if (prefix_lens[b] > maxL) maxL = prefix_lens[b];
+    }
+    for (int64_t t = 0; t < (int64_t)B * N; ++t)
+        if (N < 64 && (masks[t] >> N) != 0) return ORACLE_BAD_ARG;
+    if (rows)
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (rows[r] < 0 || rows[r] >= total_rows) return ORACLE_BAD_ARG;
+    p.max_keys = maxL + N;
     p.o = o; p.lse = lse;
     return run_rows(&p, n_threads);
 }

@@ -117,3 +117,53 @@ def attend_subset(q_vec, keys, vals, subset, scale):
     mask = [j in subset for j in range(n)]
     o, lse = _softmax_row(q_vec, keys, vals, mask, scale)
     return np.array(o), lse
+
+
+def tree_visible(parents) -> np.ndarray:
+    """Tree-attention mask, built top-down: M[i, j] = True iff i is j or lies below j.
+
+    Children lists are read off the parent array and each node's subtree is
+    walked from the node down, the reverse direction of the oracle's
+    bottom-up ancestor sets.
+    """
+    N = len(parents)
+    children = [[] for _ in range(N)]
+    for i, p in enumerate(parents):
+        if p >= 0:
+            children[int(p)].append(i)
+    vis = np.zeros((N, N), dtype=bool)
+    for j in range(N):
+        stack = [j]
+        while stack:
+            i = stack.pop()
+            vis[i, j] = True
+            stack.extend(children[i])
+    return vis
+
+
+def tree_verify(wl, part: str = "full"):
+    """Rows in oracle order: token b*N+i, then head."""
+    H_q, N = wl.H_q, wl.N
+    d = wl.head_dim
+    scale = 1.0 / math.sqrt(d)
+    q = _f64(wl.q)
+    o_rows, lse_rows = [], []
+    for b in range(wl.B):
+        L = int(wl.prefix_lens[b])
+        vis = tree_visible([int(x) for x in wl.parents[b]])
+        seq_k = np.concatenate([_expand_heads(_f64(wl.prefix_k[b]), H_q),
+                                _expand_heads(_f64(wl.tree_k[b]), H_q)], axis=0)
+        seq_v = np.concatenate([_expand_heads(_f64(wl.prefix_v[b]), H_q),
+                                _expand_heads(_f64(wl.tree_v[b]), H_q)], axis=0)
+        for i in range(N):
+            mask = [False] * (L + N)
+            for j in range(L + N):
+                if j < L:
+                    mask[j] = part != "draft"
+                else:
+                    mask[j] = part != "prefix" and bool(vis[i, j - L])
+            for h in range(H_q):
+                o, lse = _softmax_row(q[b * N + i, h], seq_k[:, h], seq_v[:, h], mask, scale)
+                o_rows.append(o)
+                lse_rows.append(lse)
+    return np.array(o_rows, dtype=np.float64).reshape(-1, d), np.array(lse_rows)
