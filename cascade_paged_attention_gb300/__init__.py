@@ -31,6 +31,9 @@ __all__ = [
     "cpa_cascade_pass_b",
     "cpa_merge_state",
     "cpa_prefill_hit",
+    "cpa_tree_verify_workspace_size",
+    "cpa_tree_verify",
+    "cpa_tree_pass_b",
     "cpa_get_device_status",
     "cpa_debug_wait_timeout",
     "cpa_plan_partition",
@@ -47,7 +50,8 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "cpa.h")
 PREFILL_FULL, PREFILL_RECT, PREFILL_TRI = 0, 1, 2
 _STATUS = {0: "CPA_OK", 1: "CPA_ERR_INVALID_ARG", 2: "CPA_ERR_UNSUPPORTED",
            3: "CPA_ERR_WORKSPACE", 4: "CPA_ERR_LAUNCH", 5: "CPA_ERR_BAD_PAGE",
-           6: "CPA_ERR_TIMEOUT", 7: "CPA_ERR_CUDA", 8: "CPA_ERR_BAD_LENGTH"}
+           6: "CPA_ERR_TIMEOUT", 7: "CPA_ERR_CUDA", 8: "CPA_ERR_BAD_LENGTH",
+           9: "CPA_ERR_BAD_TREE"}
 
 
 class CpaError(RuntimeError):
@@ -91,6 +95,10 @@ def lib() -> ctypes.CDLL:
         "cpa_cascade_pass_b": (I, [P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
         "cpa_merge_state": (I, [P, P, P, P, I, I, I, P, P, P]),
         "cpa_prefill_hit": (I, [P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P, P, P, SZ, P]),
+        "cpa_tree_verify_workspace_size": (SZ, [I, I, I, I, I, I]),
+        "cpa_tree_verify": (I, [P, P, P, P, I, P, I, P, P, I, I, I, I, I, I, I, I, F, P, P, P, SZ,
+                                P]),
+        "cpa_tree_pass_b": (I, [P, P, P, P, I, P, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
         "cpa_get_device_status": (I, [P, ctypes.POINTER(ctypes.c_uint32), P]),
         "cpa_debug_wait_timeout": (I, [P, SZ, I, P]),
         "cpa_plan_partition": (I, [I64, I, I, I64, ctypes.POINTER(ctypes.c_int64),
@@ -373,6 +381,85 @@ def cpa_prefill_hit(q, k_pages, v_pages, page_table, B: int, N: int, H_hit: int,
         _ptr(ws), ws.numel(), _stream(stream))
     _check("cpa_prefill_hit", st)
     return o, lse
+
+
+def cpa_tree_verify_workspace_size(B, N, H_q, H_kv, head_dim, page_size) -> int:
+    return lib().cpa_tree_verify_workspace_size(B, N, H_q, H_kv, head_dim, page_size)
+
+
+def _tree_shapes(q, k_pages, v_pages, tree_page_table, tree_parents):
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(tree_page_table, "tree_page_table", torch.int32, 2)
+    _need(tree_parents, "tree_parents", torch.int32, 2)
+    if k_pages.shape != v_pages.shape:
+        raise ValueError("k_pages and v_pages must have the same shape")
+    num_pages, P, H_kv, d = k_pages.shape
+    B, N = tree_parents.shape
+    T, H_q, dq = q.shape
+    if dq != d or T != B * N or tree_page_table.shape[0] != B:
+        raise ValueError("inconsistent tree verify shapes")
+    return B, N, H_q, H_kv, d, P, num_pages
+
+
+def cpa_tree_verify(q, k_pages, v_pages, prefix_page_table, tree_page_table, prefix_lens,
+                    tree_parents, max_prefix_len: Optional[int] = None,
+                    sm_scale: Optional[float] = None, o=None, lse=None, workspace=None,
+                    stream=None):
+    """Verify over draft trees (prefix pass + tree pass + merge).  Returns (o bf16, lse fp32).
+
+    ``tree_parents`` int32 [B, N]: parent BFS index of each node, -1 for a root.
+    """
+    B, N, H_q, H_kv, d, P, num_pages = _tree_shapes(q, k_pages, v_pages, tree_page_table,
+                                                     tree_parents)
+    _need(prefix_page_table, "prefix_page_table", torch.int32, 2)
+    _need(prefix_lens, "prefix_lens", torch.int32, 1)
+    if prefix_lens.numel() != B or prefix_page_table.shape[0] != B:
+        raise ValueError("inconsistent tree verify shapes")
+    if max_prefix_len is None:
+        max_prefix_len = prefix_page_table.shape[1] * P
+    if sm_scale is None:
+        sm_scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[0], H_q, dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    nbytes = cpa_tree_verify_workspace_size(B, N, H_q, H_kv, d, P)
+    ws = _workspace(nbytes, q.device, workspace)
+    st = lib().cpa_tree_verify(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(prefix_page_table),
+        prefix_page_table.shape[1], _ptr(tree_page_table), tree_page_table.shape[1],
+        _ptr(prefix_lens), _ptr(tree_parents), B, N, H_q, H_kv, d, P, num_pages,
+        int(max_prefix_len), float(sm_scale), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+        _stream(stream))
+    _check("cpa_tree_verify", st)
+    return o, lse
+
+
+def cpa_tree_pass_b(q, k_pages, v_pages, tree_page_table, tree_parents,
+                    sm_scale: Optional[float] = None, o_b=None, lse_b=None, workspace=None,
+                    stream=None):
+    """The tree part alone (each node against its ancestor-or-self nodes).  Returns fp32 (o_b, lse_b)."""
+    B, N, H_q, H_kv, d, P, num_pages = _tree_shapes(q, k_pages, v_pages, tree_page_table,
+                                                     tree_parents)
+    if sm_scale is None:
+        sm_scale = d ** -0.5
+    if o_b is None:
+        o_b = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if lse_b is None:
+        lse_b = torch.empty(q.shape[0], H_q, dtype=torch.float32, device=q.device)
+    _need(o_b, "o_b", torch.float32)
+    _need(lse_b, "lse_b", torch.float32)
+    ws = _workspace(cpa_status_workspace_size(), q.device, workspace)
+    st = lib().cpa_tree_pass_b(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(tree_page_table), tree_page_table.shape[1],
+        _ptr(tree_parents), B, N, H_q, H_kv, d, P, num_pages, float(sm_scale), _ptr(o_b),
+        _ptr(lse_b), _ptr(ws), ws.numel(), _stream(stream))
+    _check("cpa_tree_pass_b", st)
+    return o_b, lse_b
 
 
 def cpa_get_device_status(workspace: torch.Tensor, stream=None) -> tuple[int, int]:

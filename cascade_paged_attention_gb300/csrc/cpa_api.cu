@@ -84,6 +84,20 @@ WsLayout ws_layout(long long n_units, int n_sm) {
     return w;
 }
 
+// Tree verify: the prefix pass's workspace, then its fp32 result.
+struct TreeWs {
+    size_t attn, o_a, lse_a, total;
+};
+TreeWs tree_ws_layout(int B, int N, int H_q, int H_kv, int n_sm) {
+    TreeWs w;
+    w.attn = ws_layout((long long)B * H_kv, n_sm).total;
+    const size_t rows = (size_t)B * N * H_q;
+    w.o_a = w.attn;
+    w.lse_a = align_up(w.o_a + rows * 128 * 4, 256);
+    w.total = align_up(w.lse_a + rows * 4, 256);
+    return w;
+}
+
 // ---------------------------------------------------------------- launch config
 struct Geometry {
     int num_mt;
@@ -287,6 +301,7 @@ const char* cpa_status_string(cpa_status s) {
         case CPA_ERR_TIMEOUT: return "device wait timed out";
         case CPA_ERR_CUDA: return "CUDA runtime error";
         case CPA_ERR_BAD_LENGTH: return "prefix length out of range";
+        case CPA_ERR_BAD_TREE: return "tree parent index out of range";
     }
     return "unknown status";
 }
@@ -455,6 +470,112 @@ cpa_status cpa_prefill_hit(const void* q, const void* k_pages, const void* v_pag
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t cpa_tree_verify_workspace_size(int B, int N, int H_q, int H_kv, int head_dim,
+                                      int page_size) {
+    if (B < 1 || N < 1 || N > CPA_MAX_TREE_NODES || H_q < 1 || H_kv < 1 || H_q % H_kv ||
+        head_dim != 128 || !page_size_ok(page_size))
+        return 0;
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return 0;
+    return tree_ws_layout(B, N, H_q, H_kv, n_sm).total;
+}
+
+cpa_status cpa_tree_verify(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* prefix_page_table, int prefix_pt_stride,
+                           const int32_t* tree_page_table, int tree_pt_stride,
+                           const int32_t* prefix_lens, const int32_t* tree_parents, int B, int N,
+                           int H_q, int H_kv, int head_dim, int page_size, int num_pages,
+                           int max_prefix_len, float sm_scale, void* o, float* lse,
+                           void* workspace, size_t workspace_bytes, cpa_stream_t stream) {
+    // everything checkable is checked before the prefix pass launches
+    cpa_status st = check_verify(q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                                 prefix_lens, B, 1, N, H_q, H_kv, head_dim, page_size, num_pages,
+                                 max_prefix_len, sm_scale);
+    if (st != CPA_OK) return st;
+    if (!tree_page_table || !tree_parents || !o || !lse || !aligned16(o))
+        return CPA_ERR_INVALID_ARG;
+    if (N > CPA_MAX_TREE_NODES) return CPA_ERR_UNSUPPORTED;
+    if (tree_pt_stride < (N + page_size - 1) / page_size) return CPA_ERR_INVALID_ARG;
+    Geometry geo;
+    if (!plan_geometry(H_q / H_kv, N, geo)) return CPA_ERR_UNSUPPORTED;
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return CPA_ERR_CUDA;
+    const TreeWs w = tree_ws_layout(B, N, H_q, H_kv, n_sm);
+    if (!workspace || workspace_bytes < w.total) return CPA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CPA_ERR_INVALID_ARG;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* o_a = reinterpret_cast<float*>(ws + w.o_a);
+    float* lse_a = reinterpret_cast<float*>(ws + w.lse_a);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the prefix pass: all N nodes of a request are one query block (topk 1, S N)
+    st = verify_common(MODE_PASS_A, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                       nullptr, 0, prefix_lens, B, 1, N, H_q, H_kv, head_dim, page_size,
+                       num_pages, max_prefix_len, sm_scale, o_a, lse_a, workspace, w.attn, s);
+    if (st != CPA_OK) return st;
+    TreeParams tp;
+    tp.q = static_cast<const __nv_bfloat16*>(q);
+    tp.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
+    tp.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
+    tp.ttab = tree_page_table;
+    tp.ttab_stride = tree_pt_stride;
+    tp.parents = tree_parents;
+    tp.B = B;
+    tp.N = N;
+    tp.H_q = H_q;
+    tp.H_kv = H_kv;
+    tp.P = page_size;
+    tp.num_pages = num_pages;
+    tp.scale_log2 = sm_scale * kLog2e;
+    tp.o_a = o_a;
+    tp.lse_a = lse_a;
+    tp.o = o;
+    tp.lse = lse;
+    tp.status = static_cast<uint32_t*>(workspace);
+    return launch_tree(tp, s) == cudaSuccess ? CPA_OK : CPA_ERR_LAUNCH;
+}
+
+cpa_status cpa_tree_pass_b(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* tree_page_table, int tree_pt_stride,
+                           const int32_t* tree_parents, int B, int N, int H_q, int H_kv,
+                           int head_dim, int page_size, int num_pages, float sm_scale,
+                           float* o_b, float* lse_b, void* workspace, size_t workspace_bytes,
+                           cpa_stream_t stream) {
+    if (!q || !k_pages || !v_pages || !tree_page_table || !tree_parents || !o_b || !lse_b)
+        return CPA_ERR_INVALID_ARG;
+    if (B < 1 || N < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv || num_pages < 1 || page_size < 1 ||
+        !(sm_scale > 0.f) || !std::isfinite(sm_scale))
+        return CPA_ERR_INVALID_ARG;
+    if (head_dim != 128 || N > CPA_MAX_TREE_NODES) return CPA_ERR_UNSUPPORTED;
+    if (tree_pt_stride < (N + page_size - 1) / page_size) return CPA_ERR_INVALID_ARG;
+    if ((long long)B * N * H_q > (1ll << 31) / 128) return CPA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(q) & 7u) || (reinterpret_cast<uintptr_t>(k_pages) & 7u) ||
+        (reinterpret_cast<uintptr_t>(v_pages) & 7u) || !aligned16(o_b))
+        return CPA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kStatusBytes) return CPA_ERR_WORKSPACE;
+    TreeParams tp;
+    tp.q = static_cast<const __nv_bfloat16*>(q);
+    tp.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
+    tp.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
+    tp.ttab = tree_page_table;
+    tp.ttab_stride = tree_pt_stride;
+    tp.parents = tree_parents;
+    tp.B = B;
+    tp.N = N;
+    tp.H_q = H_q;
+    tp.H_kv = H_kv;
+    tp.P = page_size;
+    tp.num_pages = num_pages;
+    tp.scale_log2 = sm_scale * kLog2e;
+    tp.o_a = nullptr;
+    tp.lse_a = nullptr;
+    tp.o = o_b;
+    tp.lse = lse_b;
+    tp.status = static_cast<uint32_t*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(workspace, 0, kStatusBytes, s) != cudaSuccess) return CPA_ERR_CUDA;
+    return launch_tree(tp, s) == cudaSuccess ? CPA_OK : CPA_ERR_LAUNCH;
+}
+
 cpa_status cpa_get_device_status(const void* workspace, uint32_t* status_out,
                                   cpa_stream_t stream) {
     if (!workspace || !status_out) return CPA_ERR_INVALID_ARG;
@@ -467,6 +588,7 @@ cpa_status cpa_get_device_status(const void* workspace, uint32_t* status_out,
     if (v & CPA_DEV_TIMEOUT) return CPA_ERR_TIMEOUT;
     if (v & CPA_DEV_BAD_PAGE) return CPA_ERR_BAD_PAGE;
     if (v & CPA_DEV_BAD_LENGTH) return CPA_ERR_BAD_LENGTH;
+    if (v & CPA_DEV_BAD_TREE) return CPA_ERR_BAD_TREE;
     return CPA_OK;
 }
 

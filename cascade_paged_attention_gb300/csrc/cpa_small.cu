@@ -1,5 +1,6 @@
 // cpa_small.cu -- the light kernels of the library: merge_state, the
-// stand-alone Pass B draft kernel, and the bounded-wait check.
+// stand-alone Pass B draft kernel, the draft-tree pass, and the bounded-wait
+// check.
 #include <cuda_runtime.h>
 
 #include "cpa_device.cuh"
@@ -105,6 +106,105 @@ __global__ void __launch_bounds__(256) pass_b_kernel(PassBParams p) {
     }
 }
 
+// Draft-tree pass (KV-cache tutorial, section 8.2 tip box on tree attention,
+// and Q14): the N draft tokens of request b are a token tree flattened so that
+// every parent precedes its children (BFS order does); node i sees tree node
+// j iff j is i or one of i's ancestors.  One warp per (node, query head):
+// the warp first climbs the parent chain into a 64-bit ancestor-or-self mask
+// (at most N steps, as each step moves to a smaller index), then runs the
+// same warp-level online softmax as Pass B over the mask's nodes in
+// ascending order.  A parent index outside [-1, i) stops the climb and sets
+// CPA_DEV_BAD_TREE.  When the prefix pass's fp32 (o_a, lse_a) are given, the
+// epilogue merges the two parts by the log-sum-exp identity of the cascade
+// page and writes bf16 o; otherwise it writes its own fp32 part.
+__global__ void __launch_bounds__(256) tree_kernel(TreeParams p) {
+    const int warp_global = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int n_warps = p.B * p.N * p.H_q;
+    if (warp_global >= n_warps) return;
+    const int t = warp_global / p.H_q;  // token b*N + i
+    const int hq = warp_global % p.H_q;
+    const int hk = hq / (p.H_q / p.H_kv);
+    const int b = t / p.N, i = t % p.N;
+    const int32_t* par = p.parents + (size_t)b * p.N;
+    unsigned long long anc = 1ull << i;
+    bool bad = false;
+    for (int j = i, step = 0; step < p.N; ++step) {
+        const int pj = __ldg(par + j);
+        if (pj == -1) break;
+        if (pj < -1 || pj >= j) {
+            bad = true;
+            break;
+        }
+        anc |= 1ull << pj;
+        j = pj;
+    }
+    if (bad && lane == 0) atomicOr(p.status, CPA_DEV_BAD_TREE);
+    const int32_t* trow = p.ttab + (size_t)b * p.ttab_stride;
+    const size_t row = (size_t)t * p.H_q + hq;
+    const size_t qoff = row * 128 + lane * 4;
+    const uint2 qraw = __ldg(reinterpret_cast<const uint2*>(p.q + qoff));
+    const float q0 = __uint_as_float(qraw.x << 16), q1 = __uint_as_float(qraw.x & 0xFFFF0000u);
+    const float q2 = __uint_as_float(qraw.y << 16), q3 = __uint_as_float(qraw.y & 0xFFFF0000u);
+    float m = ninf(), l = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    for (unsigned long long rest = anc; rest != 0ull; rest &= rest - 1ull) {
+        const int j = __ffsll((long long)rest) - 1;
+        const int pg = __ldg(trow + j / p.P);
+        if (pg < 0 || pg >= p.num_pages) {
+            if (lane == 0) atomicOr(p.status, CPA_DEV_BAD_PAGE);
+            continue;
+        }
+        const size_t off = (((size_t)pg * p.P + (j % p.P)) * p.H_kv + hk) * 128 + lane * 4;
+        const uint2 kr = __ldg(reinterpret_cast<const uint2*>(p.k_pages + off));
+        const uint2 vr = __ldg(reinterpret_cast<const uint2*>(p.v_pages + off));
+        float dot = q0 * __uint_as_float(kr.x << 16) + q1 * __uint_as_float(kr.x & 0xFFFF0000u) +
+                    q2 * __uint_as_float(kr.y << 16) + q3 * __uint_as_float(kr.y & 0xFFFF0000u);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        const float x = dot * p.scale_log2;
+        const float m_new = fmaxf(m, x);
+        const float c = ex2(m - m_new);  // 0 when m is -inf
+        const float e = ex2(x - m_new);
+        l = l * c + e;
+        a0 = a0 * c + e * __uint_as_float(vr.x << 16);
+        a1 = a1 * c + e * __uint_as_float(vr.x & 0xFFFF0000u);
+        a2 = a2 * c + e * __uint_as_float(vr.y << 16);
+        a3 = a3 * c + e * __uint_as_float(vr.y & 0xFFFF0000u);
+        m = m_new;
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float lse_b = l > 0.f ? (m + lg2(l)) * kLn2F : ninf();
+    a0 *= inv;
+    a1 *= inv;
+    a2 *= inv;
+    a3 *= inv;
+    if (p.o_a == nullptr) {
+        reinterpret_cast<float4*>(static_cast<float*>(p.o) + qoff)[0] = make_float4(a0, a1, a2, a3);
+        if (lane == 0) p.lse[row] = lse_b;
+        return;
+    }
+    // merge with the prefix part about the larger log-sum-exp
+    const float la = __ldg(p.lse_a + row);
+    float wa, wb, lse;
+    if (la == ninf() && lse_b == ninf()) {
+        wa = 0.f;
+        wb = 0.f;
+        lse = ninf();
+    } else {
+        const float mx = fmaxf(la, lse_b);
+        const float ea = ex2((la - mx) * kLog2eF), eb = ex2((lse_b - mx) * kLog2eF);
+        const float s = ea + eb;
+        wa = ea / s;
+        wb = eb / s;
+        lse = mx + lg2(s) * kLn2F;
+    }
+    const float4 x = __ldg(reinterpret_cast<const float4*>(p.o_a + qoff));
+    reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + qoff)[0] =
+        make_uint2(pack_bf16x2(wa * x.x + wb * a0, wa * x.y + wb * a1),
+                   pack_bf16x2(wa * x.z + wb * a2, wa * x.w + wb * a3));
+    if (lane == 0) p.lse[row] = lse;
+}
+
 // Waits on a barrier that nothing completes; the bounded wait gives up after
 // `limit_ns`, records CPA_DEV_TIMEOUT and the kernel returns normally.
 __global__ void wait_timeout_kernel(uint32_t* status, unsigned long long limit_ns) {
@@ -137,6 +237,13 @@ cudaError_t launch_pass_b(const PassBParams& p, cudaStream_t stream) {
     const long long warps = (long long)p.B * p.topk * p.H_q;
     const long long blocks = (warps + 7) / 8;
     pass_b_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tree(const TreeParams& p, cudaStream_t stream) {
+    const long long warps = (long long)p.B * p.N * p.H_q;
+    const long long blocks = (warps + 7) / 8;
+    tree_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -24,7 +24,8 @@ import cpa_synth  # noqa: E402
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["cascade", "naive", "pass_a", "pass_b", "prefill"],
+    ap.add_argument("--case", choices=["cascade", "naive", "pass_a", "pass_b", "prefill", "tree",
+                                       "tree_pass_b"],
                     default="cascade")
     ap.add_argument("--config", default="pages_example")
     ap.add_argument("--hit", type=float, default=0.5, help="prefill: cached fraction h")
@@ -56,6 +57,23 @@ def main():
         def call():
             cpa.cpa_prefill_hit(q, kp, vp, pt, wl.B, wl.N, wl.H)
         work = f"prefill B={wl.B} N={wl.N} H={wl.H}: {wl.visible_pairs() * wl.B * wl.H_q} pairs"
+    elif args.case in ("tree", "tree_pass_b"):
+        cfg = dict(cpa_synth.TREE_CONFIGS[args.config])
+        if args.batch:
+            cfg["B"] = args.batch
+        wl = cpa_synth.make_tree_verify(**cfg)
+        q, kp, vp = bf(wl.q), bf(wl.k_pages), bf(wl.v_pages)
+        ppt, tpt, lens = i32(wl.prefix_page_table), i32(wl.tree_page_table), i32(wl.prefix_lens)
+        par = i32(wl.parents)
+        mpl = wl.max_prefix_len
+
+        def call():
+            if args.case == "tree":
+                cpa.cpa_tree_verify(q, kp, vp, ppt, tpt, lens, par, mpl)
+            else:
+                cpa.cpa_tree_pass_b(q, kp, vp, tpt, par)
+        work = (f"{args.config}: unique KV {wl.unique_kv_tokens() * wl.kv_bytes_per_token() / 1e6:.1f}"
+                f" MB")
     else:
         cfg = dict(cpa_synth.VERIFY_CONFIGS[args.config])
         if args.batch:

@@ -416,7 +416,7 @@ VERIFY_CONFIGS = {
 }
 # Draft-tree verify: the pages' example request shape (L=2000, H_q=32,
 # H_kv=8) with one 20-node tree per request in place of 4 chains of 5, and a
-# 60-node tree, the size of an EAGLE-2-style dynamic tree.
+# 60-node tree.
 TREE_CONFIGS = {
     "tree_tiny": dict(B=2, N=7, L=64, H_q=8, H_kv=2, page_size=16, seed=11),
     "tree_pages_example": dict(B=64, N=20, L=2000, H_q=32, H_kv=8, page_size=16, seed=12),

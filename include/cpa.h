@@ -75,13 +75,18 @@ typedef enum cpa_status {
     CPA_ERR_BAD_PAGE = 5,     /* device saw a page id outside [0, num_pages) */
     CPA_ERR_TIMEOUT = 6,      /* device pipeline wait exceeded its limit */
     CPA_ERR_CUDA = 7,         /* a CUDA runtime call failed */
-    CPA_ERR_BAD_LENGTH = 8    /* device saw a prefix length outside [0, max_prefix_len] */
+    CPA_ERR_BAD_LENGTH = 8,   /* device saw a prefix length outside [0, max_prefix_len] */
+    CPA_ERR_BAD_TREE = 9      /* device saw a tree parent index outside [-1, i) */
 } cpa_status;
 
 /* Bits of the device status word (first 4 bytes of a workspace). */
 #define CPA_DEV_BAD_PAGE 0x1u
 #define CPA_DEV_TIMEOUT 0x2u
 #define CPA_DEV_BAD_LENGTH 0x4u
+#define CPA_DEV_BAD_TREE 0x8u
+
+/* Largest draft tree cpa_tree_verify accepts (one 64-bit ancestor mask per node). */
+#define CPA_MAX_TREE_NODES 64
 
 /* Which part of the prefix-hit prefill to compute (cpa_prefill_hit). */
 #define CPA_PREFILL_FULL 0 /* rectangle + triangle, merged; o is bf16 */
@@ -216,10 +221,67 @@ cpa_status cpa_prefill_hit(const void* q, const void* k_pages, const void* v_pag
                            size_t workspace_bytes, cpa_stream_t stream);
 
 /*
+ * Bytes of workspace cpa_tree_verify needs for these sizes on the current
+ * device (0 for sizes it would reject).  Besides the status word and the
+ * prefix pass's merge scratch it holds the prefix pass's fp32 result,
+ * B*N*H_q*(head_dim + 1) floats.
+ */
+size_t cpa_tree_verify_workspace_size(int B, int N, int H_q, int H_kv, int head_dim,
+                                      int page_size);
+
+/*
+ * Verify over general draft trees (KV-cache tutorial, section 8.2 tip box
+ * on tree attention, and Q14): request b holds a prefix of L_b cached tokens
+ * and a draft tree of N nodes, flattened so that every parent comes before
+ * its children (BFS order does).  Node i attends the whole prefix and the
+ * tree nodes of A(i), its ancestors and itself: the mask M[i, j] = 1 iff j is
+ * in A(i), the tree generalisation of the causal mask.  The chain-per-branch
+ * case of cpa_cascade_verify is the forest of topk chains.  The prefix is
+ * read once per request for all N nodes (the cascade page's Pass A, on the
+ * tensor-core kernel), the tree nodes by a warp-level pass that also merges
+ * the two parts.
+ *   q                  bf16 [B*N, H_q, head_dim]; token b*N + i is node i of
+ *                      request b.
+ *   tree_page_table    int32 [B, tree_pt_stride]: node j of request b's tree
+ *                      is at logical position j (page j / page_size, slot
+ *                      j % page_size); tree_pt_stride >= ceil(N / page_size).
+ *   tree_parents       int32 [B, N] on the device: the BFS index of node i's
+ *                      parent, or -1 for a root (a node whose parent is the
+ *                      last prefix token; several roots make a forest).  Each
+ *                      parent index must be below its node's; the device
+ *                      sets CPA_DEV_BAD_TREE where it is not.
+ *   other arguments    as for cpa_cascade_verify (topk = 1, S = N).
+ *   o, lse             bf16 [B*N, H_q, head_dim], fp32 [B*N, H_q].
+ * Supported: head_dim 128; 1 <= N <= CPA_MAX_TREE_NODES;
+ * N*(H_q/H_kv) <= 256; page sizes as for cpa_cascade_verify.
+ */
+cpa_status cpa_tree_verify(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* prefix_page_table, int prefix_pt_stride,
+                           const int32_t* tree_page_table, int tree_pt_stride,
+                           const int32_t* prefix_lens, const int32_t* tree_parents, int B, int N,
+                           int H_q, int H_kv, int head_dim, int page_size, int num_pages,
+                           int max_prefix_len, float sm_scale, void* o, float* lse,
+                           void* workspace, size_t workspace_bytes, cpa_stream_t stream);
+
+/*
+ * The tree part of cpa_tree_verify alone: node i of request b against the
+ * tree nodes of A(i) only, one warp per (node, query head).
+ *   o_b   fp32 [B*N, H_q, head_dim];  lse_b fp32 [B*N, H_q].
+ * Workspace: at least cpa_status_workspace_size() bytes (the status word).
+ * Supported: head_dim 128; 1 <= N <= CPA_MAX_TREE_NODES.
+ */
+cpa_status cpa_tree_pass_b(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* tree_page_table, int tree_pt_stride,
+                           const int32_t* tree_parents, int B, int N, int H_q, int H_kv,
+                           int head_dim, int page_size, int num_pages, float sm_scale,
+                           float* o_b, float* lse_b, void* workspace, size_t workspace_bytes,
+                           cpa_stream_t stream);
+
+/*
  * Read the device status word of `workspace` (written by the last call that
  * used it) into *status_out (host).  SYNCHRONISES `stream`.  Returns CPA_OK
  * when the word is 0, otherwise the status matching its most serious bit
- * (TIMEOUT, then BAD_PAGE, then BAD_LENGTH).
+ * (TIMEOUT, then BAD_PAGE, then BAD_LENGTH, then BAD_TREE).
  */
 cpa_status cpa_get_device_status(const void* workspace, uint32_t* status_out,
                                   cpa_stream_t stream);

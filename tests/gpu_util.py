@@ -70,3 +70,18 @@ def sample_rows(n_rows: int, k: int, seed: int, always=()):
     pick = set(int(x) for x in rng.choice(n_rows, size=min(k, n_rows), replace=False))
     pick.update(int(a) % n_rows for a in always)
     return np.array(sorted(pick), dtype=np.int64)
+
+
+class TreeDev:
+    def __init__(self, wl, device="cuda:0"):
+        self.wl = wl
+        self.q = dev_bf16(wl.q, device)
+        self.k = dev_bf16(wl.k_pages, device)
+        self.v = dev_bf16(wl.v_pages, device)
+        self.ppt = dev_i32(wl.prefix_page_table, device)
+        self.tpt = dev_i32(wl.tree_page_table, device)
+        self.lens = dev_i32(wl.prefix_lens, device)
+        self.parents = dev_i32(wl.parents, device)
+
+    def args(self):
+        return (self.q, self.k, self.v, self.ppt, self.tpt, self.lens, self.parents)

@@ -33,8 +33,8 @@ def test_python_binding_covers_the_header(L):
 
 def test_status_strings(L):
     assert cpa.cpa_status_string(0) == "ok"
-    seen = {cpa.cpa_status_string(i) for i in range(9)}
-    assert len(seen) == 9
+    seen = {cpa.cpa_status_string(i) for i in range(10)}
+    assert len(seen) == 10
     assert cpa.cpa_status_string(99) == "unknown status"
     assert cpa.cpa_version() >= 100
 
@@ -51,6 +51,38 @@ def test_null_pointers_are_rejected_before_any_launch(L):
     assert st == 1
     st = L.cpa_get_device_status(null, None, null)
     assert st == 1
+    st = L.cpa_tree_verify(null, null, null, null, 1, null, 1, null, null, 1, 7, 8, 2, 128, 16,
+                           1, 16, 0.088, null, null, null, 0, null)
+    assert st == 1
+    st = L.cpa_tree_pass_b(null, null, null, null, 1, null, 1, 7, 8, 2, 128, 16, 1, 0.088, null,
+                           null, null, 0, null)
+    assert st == 1
+
+
+def test_tree_shape_checks_before_any_launch(L):
+    """Non-null dummy pointers that are never dereferenced: every call fails its host checks."""
+    buf = (ctypes.c_uint8 * 4096)()
+    base = ctypes.addressof(buf)
+    p = ctypes.c_void_p((base + 255) // 256 * 256)
+    # 65 nodes
+    st = L.cpa_tree_pass_b(p, p, p, p, 5, p, 1, 65, 8, 2, 128, 16, 1, 0.088, p, p, p, 4096, None)
+    assert st == 2
+    # tree table narrower than ceil(N / page_size)
+    st = L.cpa_tree_pass_b(p, p, p, p, 1, p, 1, 17, 8, 2, 128, 16, 1, 0.088, p, p, p, 4096, None)
+    assert st == 1
+    # head_dim 64
+    st = L.cpa_tree_pass_b(p, p, p, p, 1, p, 1, 7, 8, 2, 64, 16, 1, 0.088, p, p, p, 4096, None)
+    assert st == 2
+    # workspace below the status word
+    st = L.cpa_tree_pass_b(p, p, p, p, 1, p, 1, 7, 8, 2, 128, 16, 1, 0.088, p, p, p, 16, None)
+    assert st == 3
+    # tree verify: 65 nodes, then N*G > 256 rows
+    st = L.cpa_tree_verify(p, p, p, p, 1, p, 5, p, p, 1, 65, 2, 2, 128, 16, 4, 16, 0.088, p, p,
+                           p, 4096, None)
+    assert st == 2
+    st = L.cpa_tree_verify(p, p, p, p, 1, p, 4, p, p, 1, 64, 64, 8, 128, 16, 4, 16, 0.088, p, p,
+                           p, 4096, None)
+    assert st == 2
 
 
 def test_workspace_size_rejects_bad_shapes(L):
@@ -60,6 +92,9 @@ def test_workspace_size_rejects_bad_shapes(L):
     assert cpa.cpa_cascade_verify_workspace_size(1, 1, 1, 8, 2, 128, 12) == 0
     assert cpa.cpa_prefill_hit_workspace_size(1, 10, 11, 8, 2, 128, 16) == 0
     assert cpa.cpa_status_workspace_size() == 256
+    assert cpa.cpa_tree_verify_workspace_size(1, 65, 8, 2, 128, 16) == 0
+    assert cpa.cpa_tree_verify_workspace_size(1, 0, 8, 2, 128, 16) == 0
+    assert cpa.cpa_tree_verify_workspace_size(1, 7, 8, 2, 64, 16) == 0
 
 
 @pytest.mark.parametrize("total,n", [(16384, 152), (152, 152), (153, 152), (7, 3), (1, 1),
