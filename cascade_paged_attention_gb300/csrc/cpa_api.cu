@@ -548,8 +548,8 @@ cpa_status cpa_tree_pass_b(const void* q, const void* k_pages, const void* v_pag
     if (head_dim != 128 || N > CPA_MAX_TREE_NODES) return CPA_ERR_UNSUPPORTED;
     if (tree_pt_stride < (N + page_size - 1) / page_size) return CPA_ERR_INVALID_ARG;
     if ((long long)B * N * H_q > (1ll << 31) / 128) return CPA_ERR_UNSUPPORTED;
-    if ((reinterpret_cast<uintptr_t>(q) & 7u) || (reinterpret_cast<uintptr_t>(k_pages) & 7u) ||
-        (reinterpret_cast<uintptr_t>(v_pages) & 7u) || !aligned16(o_b))
+    if ((reinterpret_cast<uintptr_t>(q) & 7u) || !aligned16(k_pages) || !aligned16(v_pages) ||
+        !aligned16(o_b))
         return CPA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < kStatusBytes) return CPA_ERR_WORKSPACE;
     TreeParams tp;

@@ -265,7 +265,10 @@ cpa_status cpa_tree_verify(const void* q, const void* k_pages, const void* v_pag
 
 /*
  * The tree part of cpa_tree_verify alone: node i of request b against the
- * tree nodes of A(i) only, one warp per (node, query head).
+ * tree nodes of A(i) only.  One CTA per (request, KV head) stages that
+ * head's N tree K/V rows in shared memory; a warp then serves one node and
+ * up to 4 query heads of the group at a time.  q needs 8-byte alignment,
+ * k_pages, v_pages and o_b 16-byte alignment.
  *   o_b   fp32 [B*N, H_q, head_dim];  lse_b fp32 [B*N, H_q].
  * Workspace: at least cpa_status_workspace_size() bytes (the status word).
  * Supported: head_dim 128; 1 <= N <= CPA_MAX_TREE_NODES.

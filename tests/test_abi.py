@@ -61,7 +61,7 @@ def test_null_pointers_are_rejected_before_any_launch(L):
 
 def test_tree_shape_checks_before_any_launch(L):
     """Non-null dummy pointers that are never dereferenced: every call fails its host checks."""
-    buf = (ctypes.c_uint8 * 4096)()
+    buf = (ctypes.c_uint8 * 4352)()
     base = ctypes.addressof(buf)
     p = ctypes.c_void_p((base + 255) // 256 * 256)
     # 65 nodes
