@@ -41,6 +41,9 @@ __all__ = [
     "random_bfs_tree",
     "chain_forest",
     "TREE_CONFIGS",
+    "SharedWorkload",
+    "make_shared_verify",
+    "SHARED_CONFIGS",
     "VERIFY_CONFIGS",
     "PREFILL_CONFIG",
     "bf16_bits_from_f32",
@@ -405,6 +408,101 @@ def make_tree_verify(B: int, N: int, H_q: int, H_kv: int, head_dim: int = 128,
     return wl
 
 
+@dataclasses.dataclass
+class SharedWorkload:
+    """Multi-level verify inputs: groups of consecutive requests share one prefix.
+
+    Request b (group ``b // (B // n_groups)``) holds the group's shared prefix
+    of ``shared_len`` tokens, then its own prefix of ``prefix_lens[b]`` tokens,
+    then topk branches of S drafts.
+    """
+
+    B: int
+    n_groups: int
+    shared_len: int
+    topk: int
+    S: int
+    H_q: int
+    H_kv: int
+    head_dim: int
+    page_size: int
+    prefix_lens: np.ndarray          # int32 [B], own prefix lengths
+    q: np.ndarray                    # uint16 [B*topk*S, H_q, d]
+    k_pages: np.ndarray
+    v_pages: np.ndarray
+    shared_page_table: np.ndarray    # int32 [n_groups, ceil(shared_len/P)]
+    prefix_page_table: np.ndarray    # int32 [B, ceil(max own len/P)]
+    draft_page_table: np.ndarray     # int32 [B*topk, ceil(S/P)]
+    max_prefix_len: int
+    shared_k: Optional[list] = None  # logical K/V (optional)
+    shared_v: Optional[list] = None
+    prefix_k: Optional[list] = None
+    prefix_v: Optional[list] = None
+    draft_k: Optional[list] = None
+    draft_v: Optional[list] = None
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_pages.shape[0])
+
+    @property
+    def n_tokens(self) -> int:
+        return self.B * self.topk * self.S
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    def unique_kv_tokens(self) -> int:
+        """Each shared prefix once, each own prefix once, every branch's drafts."""
+        return (self.n_groups * self.shared_len + int(self.prefix_lens.astype(np.int64).sum())
+                + self.B * self.topk * self.S)
+
+    def kv_bytes_per_token(self) -> int:
+        return 2 * self.H_kv * self.head_dim * 2
+
+
+def make_shared_verify(B: int, n_groups: int, shared_len: int, topk: int, S: int, H_q: int,
+                       H_kv: int, head_dim: int = 128, page_size: int = 16,
+                       L: Optional[int] = None, prefix_lens=None, seed: int = 0,
+                       perm_seed: Optional[int] = None, pad_fill: str = "random",
+                       keep_logical: bool = False) -> SharedWorkload:
+    """Build one multi-level verify workload (``L`` / ``prefix_lens``: own prefix lengths)."""
+    assert B % n_groups == 0
+    rng = np.random.default_rng(seed)
+    if prefix_lens is not None:
+        lens = np.asarray(prefix_lens, dtype=np.int32).copy()
+        assert lens.shape == (B,)
+    else:
+        assert L is not None
+        lens = np.full(B, L, dtype=np.int32)
+    P = page_size
+    d = head_dim
+    q = _normal_bf16(rng, (B * topk * S, H_q, d))
+    sk = [_normal_bf16(rng, (shared_len, H_kv, d)) for _ in range(n_groups)]
+    sv = [_normal_bf16(rng, (shared_len, H_kv, d)) for _ in range(n_groups)]
+    pk = [_normal_bf16(rng, (int(lens[b]), H_kv, d)) for b in range(B)]
+    pv = [_normal_bf16(rng, (int(lens[b]), H_kv, d)) for b in range(B)]
+    dk = [_normal_bf16(rng, (S, H_kv, d)) for _ in range(B * topk)]
+    dv = [_normal_bf16(rng, (S, H_kv, d)) for _ in range(B * topk)]
+    perm_rng = np.random.default_rng(seed * 7919 + 17 if perm_seed is None else perm_seed)
+    k_pages, v_pages, tables = build_pool(sk + pk + dk, sv + pv + dv, P, perm_rng, pad_fill)
+    max_prefix_len = int(lens.max()) if B > 0 else 0
+    G_ = n_groups
+    wl = SharedWorkload(B=B, n_groups=n_groups, shared_len=shared_len, topk=topk, S=S, H_q=H_q,
+                        H_kv=H_kv, head_dim=d, page_size=P, prefix_lens=lens, q=q,
+                        k_pages=k_pages, v_pages=v_pages,
+                        shared_page_table=table_matrix(tables[:G_], (shared_len + P - 1) // P),
+                        prefix_page_table=table_matrix(tables[G_:G_ + B],
+                                                       (max_prefix_len + P - 1) // P),
+                        draft_page_table=table_matrix(tables[G_ + B:], (S + P - 1) // P),
+                        max_prefix_len=max_prefix_len)
+    if keep_logical:
+        wl.shared_k, wl.shared_v = sk, sv
+        wl.prefix_k, wl.prefix_v, wl.draft_k, wl.draft_v = pk, pv, dk, dv
+    return wl
+
+
 # The five workloads the method is exercised on, by name.  Verify shapes come
 # from the pages' example (L=2000, topk=4, S=5) and its neighbours.
 VERIFY_CONFIGS = {
@@ -421,5 +519,14 @@ TREE_CONFIGS = {
     "tree_tiny": dict(B=2, N=7, L=64, H_q=8, H_kv=2, page_size=16, seed=11),
     "tree_pages_example": dict(B=64, N=20, L=2000, H_q=32, H_kv=8, page_size=16, seed=12),
     "tree_60": dict(B=64, N=60, L=2000, H_q=32, H_kv=8, page_size=16, seed=13),
+}
+# Multi-level verify: the pages' example request shape (topk=4, S=5, 2000
+# prefix tokens per request) with the first 1024 tokens shared by all 64
+# requests (one system prompt) and 976 tokens of each request's own.
+SHARED_CONFIGS = {
+    "shared_tiny": dict(B=4, n_groups=2, shared_len=40, topk=2, S=3, L=25, H_q=8, H_kv=2,
+                        page_size=16, seed=15),
+    "shared_pages_example": dict(B=64, n_groups=1, shared_len=1024, topk=4, S=5, L=976, H_q=32,
+                                 H_kv=8, page_size=16, seed=14),
 }
 PREFILL_CONFIG = dict(B=8, N=8192, H_q=32, H_kv=8, page_size=16, seed=5, hits=(0.0, 0.5, 0.75))

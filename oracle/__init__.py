@@ -14,6 +14,14 @@ What is computed, and from which passage:
   ("Topk > 1" section of the same page).  ``part="prefix"`` / ``"draft"``
   restrict the key set to the Pass A / Pass B piece of the same page's
   two-segment decomposition.
+* ``verify_shared``: multi-level verify.  Requests whose block tables start
+  with the same physical pages share that prefix (KV-cache tutorial, the
+  block-table example of section 5.3 and ``share_prefix`` of 6.2); a group of
+  consecutive requests has one shared prefix, each request its own prefix
+  after it, each branch its own drafts.  Draft s of branch k sees all of the
+  shared prefix, all of its request's own prefix and drafts 0..s of branch k;
+  ``part`` picks one piece (``"shared"``, ``"own"``, ``"draft"``), both
+  prefixes (``"prefix"``) or everything.
 * ``ancestor_masks``: the tree-attention mask of the KV-cache tutorial
   (section 8.2 tip box; interview question Q14): tree nodes flattened in BFS
   order, A(i) = the ancestors of node i with i itself, M[i, j] = 1 iff j is in
@@ -47,7 +55,7 @@ from . import build as _build
 
 _lib = None
 
-PART_CODES = {"full": 0, "prefix": 1, "draft": 2, "rect": 1, "tri": 2}
+PART_CODES = {"full": 0, "prefix": 1, "draft": 2, "rect": 1, "tri": 2, "shared": 3, "own": 4}
 
 
 def _load():
@@ -66,6 +74,10 @@ def _load():
         lib.oracle_tree_verify.restype = i32
         lib.oracle_tree_verify.argtypes = [P, P, P, i64, P, i32, P, i32, P, P, i32, i32, i32,
                                            i32, i32, i32, i32, f64, P, i64, P, P, i32]
+        lib.oracle_verify_shared.restype = i32
+        lib.oracle_verify_shared.argtypes = [P, P, P, i64, P, i32, i32, i32, P, i32, P, i32, P,
+                                             i32, i32, i32, i32, i32, i32, i32, i32, f64, P, i64,
+                                             P, P, i32]
         lib.oracle_merge_state.restype = None
         lib.oracle_merge_state.argtypes = [P, P, P, P, i64, i32, P, P]
         _lib = lib
@@ -124,6 +136,52 @@ def verify_wl(wl, part: str = "full", rows=None, threads: int = 0):
     return verify(wl.q, wl.k_pages, wl.v_pages, wl.prefix_page_table, wl.draft_page_table,
                   wl.prefix_lens, wl.topk, wl.S, wl.H_q, wl.H_kv, part=part, rows=rows,
                   threads=threads)
+
+
+def verify_shared(q, k_pages, v_pages, shared_page_table, shared_len: int, prefix_page_table,
+                  draft_page_table, prefix_lens, topk: int, S: int, H_q: int, H_kv: int,
+                  scale: Optional[float] = None, part: str = "full",
+                  rows: Optional[Sequence[int]] = None, threads: int = 0):
+    """fp64 multi-level verify; rows and tokens as in ``verify``.
+
+    ``shared_page_table`` is int32 ``[n_groups, stride]``; request b belongs to
+    group ``b // (B // n_groups)``.
+    """
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    kp = np.ascontiguousarray(k_pages, dtype=np.uint16)
+    vp = np.ascontiguousarray(v_pages, dtype=np.uint16)
+    spt = np.ascontiguousarray(shared_page_table, dtype=np.int32)
+    ppt = np.ascontiguousarray(prefix_page_table, dtype=np.int32)
+    dpt = np.ascontiguousarray(draft_page_table, dtype=np.int32)
+    lens = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+    B = int(lens.shape[0])
+    n_groups = int(spt.shape[0])
+    if n_groups < 1 or B % n_groups:
+        raise ValueError("B must be a multiple of the number of groups")
+    d = int(q.shape[-1])
+    P = int(kp.shape[1])
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    r, rp, nr = _rows_arg(rows)
+    n = nr if r is not None else B * topk * S * H_q
+    o = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    err = lib.oracle_verify_shared(_ptr(q), _ptr(kp), _ptr(vp), int(kp.shape[0]), _ptr(spt),
+                                   int(spt.shape[1]), int(shared_len), B // n_groups, _ptr(ppt),
+                                   int(ppt.shape[1]), _ptr(dpt), int(dpt.shape[1]), _ptr(lens), B,
+                                   topk, S, H_q, H_kv, d, P, PART_CODES[part], float(scale), rp,
+                                   nr, _ptr(o), _ptr(lse), threads)
+    if err:
+        raise ValueError(f"oracle_verify_shared: {_ERR.get(err, err)}")
+    return o, lse
+
+
+def verify_shared_wl(wl, part: str = "full", rows=None, threads: int = 0):
+    """``verify_shared`` on a ``cpa_synth.SharedWorkload``-shaped object."""
+    return verify_shared(wl.q, wl.k_pages, wl.v_pages, wl.shared_page_table, wl.shared_len,
+                         wl.prefix_page_table, wl.draft_page_table, wl.prefix_lens, wl.topk,
+                         wl.S, wl.H_q, wl.H_kv, part=part, rows=rows, threads=threads)
 
 
 def ancestor_masks(parents) -> np.ndarray:

@@ -107,7 +107,8 @@ static void attend_one(const double *q, const uint16_t *k_pages, const uint16_t 
 
 enum { KIND_VERIFY = 0, KIND_PREFILL = 1, KIND_TREE = 2 };
 /* part: 0 = full visible set, 1 = first piece only (prefix / rectangle),
- *       2 = second piece only (own drafts / causal triangle).            */
+ *       2 = second piece only (own drafts / causal triangle);
+ *       multi-level verify also: 3 = shared prefix only, 4 = own prefix only. */
 
 typedef struct {
     int kind;
@@ -119,6 +120,9 @@ typedef struct {
     /* verify */
     const int32_t *prefix_pt, *draft_pt, *prefix_lens;
     int prefix_stride, draft_stride, B, topk, S;
+    /* multi-level verify: one shared prefix per group of group_size requests */
+    const int32_t *shared_pt;
+    int shared_stride, shared_len, group_size;
     /* tree verify (also uses prefix_pt, prefix_stride, prefix_lens, B, N) */
     const int32_t *tree_pt;
     int tree_stride;
@@ -156,12 +160,22 @@ static int visible_keys(const problem_t *p, int64_t token, int head, int64_t *ke
         int i = (int)(token % TS);
         int branch = i / p->S;
         int s = i % p->S;
-        if (p->part != 2) {
+        /* pieces in key order: the group's shared prefix (multi-level only), the
+         * request's own prefix, the branch's own drafts */
+        int want_shared = p->part == 0 || p->part == 1 || p->part == 3;
+        int want_own = p->part == 0 || p->part == 1 || p->part == 4;
+        int want_draft = p->part == 0 || p->part == 2;
+        if (p->shared_pt && want_shared) {
+            const int32_t *row = p->shared_pt + (int64_t)(b / p->group_size) * p->shared_stride;
+            for (int pos = 0; pos < p->shared_len; ++pos)
+                key_off[n++] = key_offset(p, row, pos, kv_head, &bad);
+        }
+        if (want_own) {
             const int32_t *row = p->prefix_pt + (int64_t)b * p->prefix_stride;
             int L = p->prefix_lens[b];
             for (int pos = 0; pos < L; ++pos) key_off[n++] = key_offset(p, row, pos, kv_head, &bad);
         }
-        if (p->part != 1) {
+        if (want_draft) {
             const int32_t *row = p->draft_pt + ((int64_t)b * p->topk + branch) * p->draft_stride;
             for (int j = 0; j <= s; ++j) key_off[n++] = key_offset(p, row, j, kv_head, &bad);
         }
@@ -285,6 +299,55 @@ int oracle_verify(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_
         for (int64_t r = 0; r < n_rows; ++r)
             if (rows[r] < 0 || rows[r] >= total_rows) return ORACLE_BAD_ARG;
     p.max_keys = maxL + S;
+    p.o = o; p.lse = lse;
+    return run_rows(&p, n_threads);
+}
+
+/*
+ * Multi-level verify (KV-cache tutorial, sections 5.3 and 6.2: requests whose
+ * block tables begin with the same physical pages share that prefix).  The
+ * B requests form B / group_size groups of consecutive requests; group g's
+ * shared prefix is positions 0..shared_len-1 of shared_pt row g.  Request b
+ * then has its own prefix (prefix_pt row b, prefix_lens[b] tokens) and its
+ * branches' drafts as in oracle_verify.  Draft s of branch k of request b
+ * sees the shared prefix, the own prefix and drafts 0..s of its branch.
+ * part 0 = all, 1 = shared + own prefix, 2 = drafts, 3 = shared only,
+ * 4 = own prefix only.
+ */
+int oracle_verify_shared(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                         int64_t num_pages, const int32_t *shared_pt, int shared_stride,
+                         int shared_len, int group_size, const int32_t *prefix_pt,
+                         int prefix_stride, const int32_t *draft_pt, int draft_stride,
+                         const int32_t *prefix_lens, int B, int topk, int S, int H_q, int H_kv,
+                         int d, int P, int part, double scale, const int64_t *rows,
+                         int64_t n_rows, double *o, double *lse, int n_threads) {
+    if (B < 0 || topk < 1 || S < 1 || H_kv < 1 || H_q % H_kv != 0 || d < 1 || P < 1 ||
+        part < 0 || part > 4 || !shared_pt || shared_len < 0 || group_size < 1 ||
+        B % group_size != 0)
+        return ORACLE_BAD_ARG;
+    problem_t p;
+    memset(&p, 0, sizeof p);
+    p.kind = KIND_VERIFY;
+    p.part = part;
+    p.q = q; p.k_pages = k_pages; p.v_pages = v_pages; p.num_pages = num_pages;
+    p.H_q = H_q; p.H_kv = H_kv; p.d = d; p.P = P; p.scale = scale;
+    p.shared_pt = shared_pt; p.shared_stride = shared_stride; p.shared_len = shared_len;
+    p.group_size = group_size;
+    p.prefix_pt = prefix_pt; p.draft_pt = draft_pt; p.prefix_lens = prefix_lens;
+    p.prefix_stride = prefix_stride; p.draft_stride = draft_stride;
+    p.B = B; p.topk = topk; p.S = S;
+    int64_t total_rows = (int64_t)B * topk * S * H_q;
+    p.rows = rows;
+    p.n_rows = rows ? n_rows : total_rows;
+    int maxL = 0;
+    for (int b = 0; b < B; ++b) {
+        if (prefix_lens[b] < 0) return ORACLE_BAD_ARG;
+        if (prefix_lens[b] > maxL) maxL = prefix_lens[b];
+    }
+    if (rows)
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (rows[r] < 0 || rows[r] >= total_rows) return ORACLE_BAD_ARG;
+    p.max_keys = shared_len + maxL + S;
     p.o = o; p.lse = lse;
     return run_rows(&p, n_threads);
 }

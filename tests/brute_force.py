@@ -167,3 +167,38 @@ def tree_verify(wl, part: str = "full"):
                 o_rows.append(o)
                 lse_rows.append(lse)
     return np.array(o_rows, dtype=np.float64).reshape(-1, d), np.array(lse_rows)
+
+
+def verify_shared(wl, part: str = "full"):
+    """Multi-level verify on logical sequences; rows in oracle order."""
+    H_q, S, topk = wl.H_q, wl.S, wl.topk
+    d = wl.head_dim
+    scale = 1.0 / math.sqrt(d)
+    q = _f64(wl.q)
+    R = wl.B // wl.n_groups
+    Ls = wl.shared_len
+    o_rows, lse_rows = [], []
+    for b in range(wl.B):
+        g = b // R
+        L = int(wl.prefix_lens[b])
+        for k in range(topk):
+            # the sequence this branch would hold: shared prefix, own prefix, own drafts
+            parts_k = [wl.shared_k[g], wl.prefix_k[b], wl.draft_k[b * topk + k]]
+            parts_v = [wl.shared_v[g], wl.prefix_v[b], wl.draft_v[b * topk + k]]
+            seq_k = np.concatenate([_expand_heads(_f64(x), H_q) for x in parts_k], axis=0)
+            seq_v = np.concatenate([_expand_heads(_f64(x), H_q) for x in parts_v], axis=0)
+            for s in range(S):
+                t = (b * topk + k) * S + s
+                mask = []
+                for j in range(Ls + L + S):
+                    if j < Ls:
+                        mask.append(part in ("full", "prefix", "shared"))
+                    elif j < Ls + L:
+                        mask.append(part in ("full", "prefix", "own"))
+                    else:
+                        mask.append(part in ("full", "draft") and (j - Ls - L) <= s)
+                for h in range(H_q):
+                    o, lse = _softmax_row(q[t, h], seq_k[:, h], seq_v[:, h], mask, scale)
+                    o_rows.append(o)
+                    lse_rows.append(lse)
+    return np.array(o_rows, dtype=np.float64).reshape(-1, d), np.array(lse_rows)

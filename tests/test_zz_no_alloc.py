@@ -14,7 +14,9 @@ import torch
 
 import cascade_paged_attention_gb300 as cpa
 import cpa_synth
-from tests.gpu_util import TOL_LSE, TOL_O, VerifyDev
+import oracle
+from tests.gpu_util import TOL_LSE, TOL_O, VerifyDev, compare
+from tests.test_gpu_graph import _load, _static_buffers
 
 pytestmark = pytest.mark.gpu
 
@@ -56,3 +58,32 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(cuda_device):
                                         H_q, H_kv, 128, 16, 1, 16, 0.088, p(q), p(i), None)
     assert st == 3  # CPA_ERR_WORKSPACE
     assert cpa.cpa_status_string(st) == "workspace missing or too small"
+
+
+def test_noalloc_graph_replay(cuda_device):
+    """The static-scratch call captured once and replayed over new lengths."""
+    B, topk, S, H_q, H_kv, P, max_len = 4, 2, 3, 16, 4, 16, 600
+    steps = [cpa_synth.make_verify(B=B, topk=topk, S=S, H_q=H_q, H_kv=H_kv, page_size=P,
+                                   prefix_lens=lens, seed=300 + i)
+             for i, lens in enumerate([[600, 1, 0, 333], [17, 600, 250, 5]])]
+    bufs, _ = _static_buffers(steps, cuda_device)
+    o = torch.empty_like(bufs["q"])
+    lse = torch.empty(bufs["q"].shape[0], H_q, dtype=torch.float32, device=cuda_device)
+
+    def call():
+        cpa.cpa_cascade_verify_noalloc(bufs["q"], bufs["k"], bufs["v"], bufs["ppt"], bufs["dpt"],
+                                       bufs["lens"], topk, S, o, lse, max_prefix_len=max_len)
+
+    _load(bufs, steps[0])
+    call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    for wl in steps:
+        _load(bufs, wl)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        compare(o, lse, *oracle.verify_wl(wl))
