@@ -31,6 +31,8 @@ __all__ = [
     "cpa_cascade_pass_b",
     "cpa_merge_state",
     "cpa_prefill_hit",
+    "cpa_cascade_verify_shared_workspace_size",
+    "cpa_cascade_verify_shared",
     "cpa_tree_verify_workspace_size",
     "cpa_tree_verify",
     "cpa_tree_pass_b",
@@ -95,6 +97,9 @@ def lib() -> ctypes.CDLL:
         "cpa_cascade_pass_b": (I, [P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
         "cpa_merge_state": (I, [P, P, P, P, I, I, I, P, P, P]),
         "cpa_prefill_hit": (I, [P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P, P, P, SZ, P]),
+        "cpa_cascade_verify_shared_workspace_size": (SZ, [I, I, I, I, I, I, I, I]),
+        "cpa_cascade_verify_shared": (I, [P, P, P, P, I, I, I, P, I, P, I, P, I, I, I, I, I, I,
+                                          I, I, I, F, P, P, P, SZ, P]),
         "cpa_tree_verify_workspace_size": (SZ, [I, I, I, I, I, I]),
         "cpa_tree_verify": (I, [P, P, P, P, I, P, I, P, P, I, I, I, I, I, I, I, I, F, P, P, P, SZ,
                                 P]),
@@ -380,6 +385,52 @@ def cpa_prefill_hit(q, k_pages, v_pages, page_table, B: int, N: int, H_hit: int,
         H_hit, H_q, H_kv, d, P, num_pages, float(sm_scale), int(part), _ptr(o), _ptr(lse),
         _ptr(ws), ws.numel(), _stream(stream))
     _check("cpa_prefill_hit", st)
+    return o, lse
+
+
+def cpa_cascade_verify_shared_workspace_size(B, n_groups, topk, S, H_q, H_kv, head_dim,
+                                            page_size) -> int:
+    return lib().cpa_cascade_verify_shared_workspace_size(B, n_groups, topk, S, H_q, H_kv,
+                                                          head_dim, page_size)
+
+
+def cpa_cascade_verify_shared(q, k_pages, v_pages, shared_page_table, shared_len: int,
+                              prefix_page_table, draft_page_table, prefix_lens, topk: int, S: int,
+                              max_prefix_len: Optional[int] = None,
+                              sm_scale: Optional[float] = None, o=None, lse=None, workspace=None,
+                              stream=None):
+    """Multi-level cascade verify.  Returns (o bf16, lse fp32).
+
+    ``shared_page_table`` int32 [n_groups, stride]: one shared prefix of
+    ``shared_len`` tokens per group of ``B // n_groups`` consecutive requests;
+    ``prefix_page_table`` / ``prefix_lens`` describe each request's own prefix.
+    """
+    B, H_q, H_kv, d, P, num_pages = _verify_shapes(q, k_pages, v_pages, prefix_page_table,
+                                                    prefix_lens, topk, S)
+    _need(shared_page_table, "shared_page_table", torch.int32, 2)
+    _need(draft_page_table, "draft_page_table", torch.int32, 2)
+    n_groups = shared_page_table.shape[0]
+    if draft_page_table.shape[0] != B * topk or n_groups < 1 or B % n_groups:
+        raise ValueError("inconsistent multi-level verify shapes")
+    if max_prefix_len is None:
+        max_prefix_len = prefix_page_table.shape[1] * P
+    if sm_scale is None:
+        sm_scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[0], H_q, dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    nbytes = cpa_cascade_verify_shared_workspace_size(B, n_groups, topk, S, H_q, H_kv, d, P)
+    ws = _workspace(nbytes, q.device, workspace)
+    st = lib().cpa_cascade_verify_shared(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(shared_page_table),
+        shared_page_table.shape[1], n_groups, int(shared_len), _ptr(prefix_page_table),
+        prefix_page_table.shape[1], _ptr(draft_page_table), draft_page_table.shape[1],
+        _ptr(prefix_lens), B, topk, S, H_q, H_kv, d, P, num_pages, int(max_prefix_len),
+        float(sm_scale), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _check("cpa_cascade_verify_shared", st)
     return o, lse
 
 

@@ -98,6 +98,29 @@ TreeWs tree_ws_layout(int B, int N, int H_q, int H_kv, int n_sm) {
     return w;
 }
 
+// Multi-level verify: the larger of the two launches' workspaces, then the
+// shared level's and the own level's fp32 partials.
+struct SharedWs {
+    size_t attn, o1, lse1, o2, lse2, total;
+};
+SharedWs shared_ws_layout(int B, int n_groups, int topk, int S, int H_q, int H_kv, int n_sm) {
+    SharedWs w;
+    const int G = H_q / H_kv;
+    const int TS = 128 / G;
+    const long long M = (long long)(B / n_groups) * topk * S;
+    const long long QT = (M + TS - 1) / TS;
+    const size_t a1 = ws_layout((long long)n_groups * H_kv * QT, n_sm).total;
+    const size_t a2 = ws_layout((long long)B * H_kv, n_sm).total;
+    const size_t rows = (size_t)B * topk * S * H_q;
+    w.attn = a1 > a2 ? a1 : a2;
+    w.o1 = w.attn;
+    w.lse1 = align_up(w.o1 + rows * 128 * 4, 256);
+    w.o2 = align_up(w.lse1 + rows * 4, 256);
+    w.lse2 = align_up(w.o2 + rows * 128 * 4, 256);
+    w.total = align_up(w.lse2 + rows * 4, 256);
+    return w;
+}
+
 // ---------------------------------------------------------------- launch config
 struct Geometry {
     int num_mt;
@@ -154,8 +177,11 @@ cudaError_t launch_attn(const AttnParams& p, int smem, int grid, cudaStream_t st
     return cudaGetLastError();
 }
 
+// keep_status: the call is the second launch of one entry point, whose first
+// launch already cleared the status word (clearing it again would drop that
+// launch's bits); only the merge counters are cleared.
 cpa_status run_attn(AttnParams& p, const Geometry& geo, long long n_units, void* workspace,
-                    size_t ws_bytes, cudaStream_t stream) {
+                    size_t ws_bytes, cudaStream_t stream, bool keep_status = false) {
     const int n_sm = sm_count();
     if (n_sm <= 0) return CPA_ERR_CUDA;
     const WsLayout wl = ws_layout(n_units, n_sm);
@@ -174,7 +200,9 @@ cpa_status run_attn(AttnParams& p, const Geometry& geo, long long n_units, void*
     p.n_qbufs = geo.n_qbufs;
     p.off_q = geo.off_q;
     p.off_kv = geo.off_kv;
-    if (cudaMemsetAsync(workspace, 0, wl.part_lse, stream) != cudaSuccess) return CPA_ERR_CUDA;
+    const size_t clear0 = keep_status ? wl.counters : 0;
+    if (cudaMemsetAsync(ws + clear0, 0, wl.part_lse - clear0, stream) != cudaSuccess)
+        return CPA_ERR_CUDA;
     cudaError_t e = geo.num_mt == 1 ? launch_attn<1>(p, geo.smem_bytes, n_sm, stream)
                                     : launch_attn<2>(p, geo.smem_bytes, n_sm, stream);
     return e == cudaSuccess ? CPA_OK : CPA_ERR_LAUNCH;
@@ -235,12 +263,14 @@ bool kv_maps(AttnParams& p, const void* k_pages, const void* v_pages, int H_kv, 
            make_map(&p.vmap, v_pages, H_kv, rows, 1, p.boxr);
 }
 
+// f32_out: o receives the fp32 result (always for Pass A; for cascade when the
+// result is a partial that a later launch merges).  keep_status: see run_attn.
 cpa_status verify_common(int mode, const void* q, const void* k_pages, const void* v_pages,
                          const int32_t* ppt, int ppt_stride, const int32_t* dpt, int dpt_stride,
                          const int32_t* lens, int B, int topk, int S, int H_q, int H_kv,
                          int head_dim, int page_size, int num_pages, int max_prefix_len,
                          float sm_scale, void* o, float* lse, void* workspace, size_t ws_bytes,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, bool f32_out = false, bool keep_status = false) {
     cpa_status st = check_verify(q, k_pages, v_pages, ppt, ppt_stride, lens, B, topk, S, H_q, H_kv,
                                  head_dim, page_size, num_pages, max_prefix_len, sm_scale);
     if (st != CPA_OK) return st;
@@ -262,6 +292,7 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
     fill_common(p, q, k_pages, v_pages, ppt, ppt_stride, dpt, dpt_stride, lens, B, topk, S, H_q,
                 H_kv, page_size, num_pages, max_prefix_len, sm_scale);
     p.mode = mode;
+    p.out_f32 = (mode == MODE_PASS_A || f32_out) ? 1 : 0;
     p.upg = mode == MODE_NAIVE ? topk * H_kv : H_kv;
     p.has_draft = draft ? 1 : 0;
     p.sb = sb;
@@ -280,7 +311,7 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
             return CPA_ERR_CUDA;
     }
     const long long n_units = (long long)B * p.upg;
-    return run_attn(p, geo, n_units, workspace, ws_bytes, stream);
+    return run_attn(p, geo, n_units, workspace, ws_bytes, stream, keep_status);
 }
 
 }  // namespace
@@ -457,6 +488,7 @@ cpa_status cpa_prefill_hit(const void* q, const void* k_pages, const void* v_pag
     p.mode = part == CPA_PREFILL_FULL ? MODE_PREFILL
              : part == CPA_PREFILL_RECT ? MODE_PREFILL_RECT
                                         : MODE_PREFILL_TRI;
+    p.out_f32 = part != CPA_PREFILL_FULL ? 1 : 0;
     p.N = N;
     p.H_hit = H_hit;
     p.M = M;
@@ -468,6 +500,95 @@ cpa_status cpa_prefill_hit(const void* q, const void* k_pages, const void* v_pag
     const long long n_units = (long long)B * H_kv * p.QT;
     return run_attn(p, geo, n_units, workspace, workspace_bytes,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t cpa_cascade_verify_shared_workspace_size(int B, int n_groups, int topk, int S, int H_q,
+                                                int H_kv, int head_dim, int page_size) {
+    if (B < 1 || n_groups < 1 || B % n_groups || topk < 1 || S < 1 || H_q < 1 || H_kv < 1 ||
+        H_q % H_kv || head_dim != 128 || !page_size_ok(page_size))
+        return 0;
+    if (!pow2(H_q / H_kv) || H_q / H_kv > 128) return 0;
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return 0;
+    return shared_ws_layout(B, n_groups, topk, S, H_q, H_kv, n_sm).total;
+}
+
+cpa_status cpa_cascade_verify_shared(const void* q, const void* k_pages, const void* v_pages,
+                                     const int32_t* shared_page_table, int shared_pt_stride,
+                                     int n_groups, int shared_len,
+                                     const int32_t* prefix_page_table, int prefix_pt_stride,
+                                     const int32_t* draft_page_table, int draft_pt_stride,
+                                     const int32_t* prefix_lens, int B, int topk, int S, int H_q,
+                                     int H_kv, int head_dim, int page_size, int num_pages,
+                                     int max_prefix_len, float sm_scale, void* o, float* lse,
+                                     void* workspace, size_t workspace_bytes,
+                                     cpa_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // everything checkable is checked before the first launch
+    cpa_status st = check_verify(q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                                 prefix_lens, B, topk, S, H_q, H_kv, head_dim, page_size,
+                                 num_pages, max_prefix_len, sm_scale);
+    if (st != CPA_OK) return st;
+    if (!o || !lse || !aligned16(o) || n_groups < 1 || B % n_groups || shared_len < 0)
+        return CPA_ERR_INVALID_ARG;
+    if (shared_len == 0)  // one level less: plain cascade verify
+        return verify_common(MODE_CASCADE, q, k_pages, v_pages, prefix_page_table,
+                             prefix_pt_stride, draft_page_table, draft_pt_stride, prefix_lens, B,
+                             topk, S, H_q, H_kv, head_dim, page_size, num_pages, max_prefix_len,
+                             sm_scale, o, lse, workspace, workspace_bytes, s);
+    if (!shared_page_table || shared_pt_stride < (shared_len + page_size - 1) / page_size)
+        return CPA_ERR_INVALID_ARG;
+    const int sb = S <= 8 ? 8 : 16;
+    if (!draft_page_table || draft_pt_stride < (S + page_size - 1) / page_size)
+        return CPA_ERR_INVALID_ARG;
+    if (S > kMaxDraft || S > page_size || topk * sb > kBN) return CPA_ERR_UNSUPPORTED;
+    const int G = H_q / H_kv;
+    Geometry geo1, geo2;
+    if (!plan_geometry(G, 128 / G, geo1) || !plan_geometry(G, topk * S, geo2))
+        return CPA_ERR_UNSUPPORTED;
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return CPA_ERR_CUDA;
+    const SharedWs w = shared_ws_layout(B, n_groups, topk, S, H_q, H_kv, n_sm);
+    if (!workspace || workspace_bytes < w.total) return CPA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CPA_ERR_INVALID_ARG;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* o1 = reinterpret_cast<float*>(ws + w.o1);
+    float* lse1 = reinterpret_cast<float*>(ws + w.lse1);
+    float* o2 = reinterpret_cast<float*>(ws + w.o2);
+    float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
+
+    // level 1: the group's draft queries (consecutive tokens) against its shared
+    // prefix, read once per group: the rectangle of a prefix-hit prefill whose
+    // M suffix queries are the group's tokens and whose sequence ends with the
+    // shared prefix (so no key past it is loaded)
+    const int M = (B / n_groups) * topk * S;
+    const int TS = 128 / G;
+    AttnParams p;
+    fill_common(p, q, k_pages, v_pages, shared_page_table, shared_pt_stride, nullptr, 0, nullptr,
+                n_groups, 1, 1, H_q, H_kv, page_size, num_pages, 0, sm_scale);
+    p.mode = MODE_PREFILL_RECT;
+    p.out_f32 = 1;
+    p.N = shared_len;
+    p.H_hit = shared_len;
+    p.M = M;
+    p.QT = (M + TS - 1) / TS;
+    p.o = o1;
+    p.lse = lse1;
+    if (!make_map(&p.qmap, q, H_q, (uint64_t)n_groups * M, G, geo1.TSB)) return CPA_ERR_CUDA;
+    if (!kv_maps(p, k_pages, v_pages, H_kv, num_pages, page_size)) return CPA_ERR_CUDA;
+    st = run_attn(p, geo1, (long long)n_groups * H_kv * p.QT, workspace, w.attn, s);
+    if (st != CPA_OK) return st;
+    // level 2: own prefix + drafts, the fused cascade kernel, fp32 partial
+    st = verify_common(MODE_CASCADE, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                       draft_page_table, draft_pt_stride, prefix_lens, B, topk, S, H_q, H_kv,
+                       head_dim, page_size, num_pages, max_prefix_len, sm_scale, o2, lse2,
+                       workspace, w.attn, s, /*f32_out=*/true, /*keep_status=*/true);
+    if (st != CPA_OK) return st;
+    // level 3: merge
+    const long long rows = (long long)B * topk * S * H_q;
+    return launch_merge_state(o1, lse1, o2, lse2, rows, 128, o, lse, n_sm, s) == cudaSuccess
+               ? CPA_OK
+               : CPA_ERR_LAUNCH;
 }
 
 size_t cpa_tree_verify_workspace_size(int B, int N, int H_q, int H_kv, int head_dim,

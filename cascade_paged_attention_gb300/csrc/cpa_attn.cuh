@@ -100,6 +100,7 @@ struct AttnParams {
     int has_draft;        // cascade / naive: the unit's drafts form its last tile
     int sb;               // rows per branch block in the draft tile (8 or 16)
     int nbr;              // branches per unit (cascade topk, naive 1)
+    int out_f32;          // o is fp32 (a partial for a later merge) instead of bf16
     float scale_log2;     // sm_scale * log2(e)
     uint32_t off_q, off_kv;
 };
@@ -1100,8 +1101,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             const int r = quarter * 32 + lane;
             const int et = r;  // 0..127 within the epilogue warpgroup
             const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-            const bool fp32_out = p.mode == MODE_PASS_A || p.mode == MODE_PREFILL_RECT ||
-                                  p.mode == MODE_PREFILL_TRI;
+            const bool fp32_out = p.out_f32 != 0;
             // Q of one unit into TMEM buffer qb: row r is query token r / G, head r % G
             auto load_q = [&](const Unit& xu, int qb) {
                 const int it = r / G, gq = r % G;

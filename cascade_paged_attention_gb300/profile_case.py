@@ -25,7 +25,7 @@ import cpa_synth  # noqa: E402
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", choices=["cascade", "naive", "pass_a", "pass_b", "prefill", "tree",
-                                       "tree_pass_b"],
+                                       "tree_pass_b", "shared"],
                     default="cascade")
     ap.add_argument("--config", default="pages_example")
     ap.add_argument("--hit", type=float, default=0.5, help="prefill: cached fraction h")
@@ -57,6 +57,19 @@ def main():
         def call():
             cpa.cpa_prefill_hit(q, kp, vp, pt, wl.B, wl.N, wl.H)
         work = f"prefill B={wl.B} N={wl.N} H={wl.H}: {wl.visible_pairs() * wl.B * wl.H_q} pairs"
+    elif args.case == "shared":
+        cfg = dict(cpa_synth.SHARED_CONFIGS[args.config])
+        wl = cpa_synth.make_shared_verify(**cfg)
+        q, kp, vp = bf(wl.q), bf(wl.k_pages), bf(wl.v_pages)
+        spt, ppt = i32(wl.shared_page_table), i32(wl.prefix_page_table)
+        dpt, lens = i32(wl.draft_page_table), i32(wl.prefix_lens)
+        mpl = wl.max_prefix_len
+
+        def call():
+            cpa.cpa_cascade_verify_shared(q, kp, vp, spt, wl.shared_len, ppt, dpt, lens, wl.topk,
+                                          wl.S, mpl)
+        work = (f"{args.config}: unique KV {wl.unique_kv_tokens() * wl.kv_bytes_per_token() / 1e6:.1f}"
+                f" MB")
     elif args.case in ("tree", "tree_pass_b"):
         cfg = dict(cpa_synth.TREE_CONFIGS[args.config])
         if args.batch:

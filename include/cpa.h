@@ -221,6 +221,51 @@ cpa_status cpa_prefill_hit(const void* q, const void* k_pages, const void* v_pag
                            size_t workspace_bytes, cpa_stream_t stream);
 
 /*
+ * Bytes of workspace cpa_cascade_verify_shared needs for these sizes on the
+ * current device (0 for sizes it would reject).  Besides the status word and
+ * merge scratch it holds two fp32 partial results, 2*B*topk*S*H_q*
+ * (head_dim + 1) floats.
+ */
+size_t cpa_cascade_verify_shared_workspace_size(int B, int n_groups, int topk, int S, int H_q,
+                                                int H_kv, int head_dim, int page_size);
+
+/*
+ * Multi-level cascade verify.  Requests whose block tables begin with the
+ * same physical pages share that prefix (KV-cache tutorial, block-table
+ * example of section 5.3; share_prefix of section 6.2), e.g. one system
+ * prompt for a whole batch.  The B requests form n_groups groups of
+ * B/n_groups consecutive requests; each group has one shared prefix of
+ * shared_len tokens, each request then its own prefix, each branch its own
+ * drafts.  Draft s of branch k of request b sees the group's shared prefix,
+ * request b's own prefix and drafts 0..s of branch k.  Three levels, merged
+ * by the cascade page's log-sum-exp identity: the shared prefix is read once
+ * per group for all the group's draft queries (the tensor-core kernel in its
+ * rectangle mode, the group's queries as one block of suffix queries), the
+ * own prefix once per request and the drafts once per branch (the fused
+ * cascade kernel), then one merge.
+ *   shared_page_table  int32 [n_groups, shared_pt_stride]: the group's shared
+ *                      pages; shared_pt_stride >= ceil(shared_len/page_size).
+ *                      May be NULL when shared_len is 0.
+ *   shared_len         host: shared prefix length of every group (>= 0).
+ *   prefix_page_table, prefix_lens
+ *                      each request's own prefix (the tokens after the shared
+ *                      part), own position j at page row[j / page_size], slot
+ *                      j % page_size; max_prefix_len bounds prefix_lens.
+ *   other arguments    as for cpa_cascade_verify.
+ * Supported: as for cpa_cascade_verify, and B a multiple of n_groups.
+ */
+cpa_status cpa_cascade_verify_shared(const void* q, const void* k_pages, const void* v_pages,
+                                     const int32_t* shared_page_table, int shared_pt_stride,
+                                     int n_groups, int shared_len,
+                                     const int32_t* prefix_page_table, int prefix_pt_stride,
+                                     const int32_t* draft_page_table, int draft_pt_stride,
+                                     const int32_t* prefix_lens, int B, int topk, int S, int H_q,
+                                     int H_kv, int head_dim, int page_size, int num_pages,
+                                     int max_prefix_len, float sm_scale, void* o, float* lse,
+                                     void* workspace, size_t workspace_bytes,
+                                     cpa_stream_t stream);
+
+/*
  * Bytes of workspace cpa_tree_verify needs for these sizes on the current
  * device (0 for sizes it would reject).  Besides the status word and the
  * prefix pass's merge scratch it holds the prefix pass's fp32 result,
