@@ -59,6 +59,35 @@ def test_null_pointers_are_rejected_before_any_launch(L):
     assert st == 1
 
 
+def test_shared_verify_checks_before_any_launch(L):
+    """Multi-level verify: bad groupings and tables fail their host checks, nothing launches."""
+    buf = (ctypes.c_uint8 * 4352)()
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 255) // 256 * 256)
+    null = None
+    # null q
+    st = L.cpa_cascade_verify_shared(null, p, p, p, 4, 1, 64, p, 1, p, 1, p, 4, 2, 3, 8, 2, 128,
+                                     16, 8, 16, 0.088, p, p, p, 4096, None)
+    assert st == 1
+    # B = 4 is not a multiple of 3 groups
+    st = L.cpa_cascade_verify_shared(p, p, p, p, 4, 3, 64, p, 1, p, 1, p, 4, 2, 3, 8, 2, 128, 16,
+                                     8, 16, 0.088, p, p, p, 4096, None)
+    assert st == 1
+    # shared table narrower than ceil(shared_len / page_size)
+    st = L.cpa_cascade_verify_shared(p, p, p, p, 3, 2, 64, p, 1, p, 1, p, 4, 2, 3, 8, 2, 128, 16,
+                                     8, 16, 0.088, p, p, p, 4096, None)
+    assert st == 1
+    # negative shared length
+    st = L.cpa_cascade_verify_shared(p, p, p, p, 4, 2, -1, p, 1, p, 1, p, 4, 2, 3, 8, 2, 128, 16,
+                                     8, 16, 0.088, p, p, p, 4096, None)
+    assert st == 1
+    # head_dim 64
+    st = L.cpa_cascade_verify_shared(p, p, p, p, 4, 2, 64, p, 1, p, 1, p, 4, 2, 3, 8, 2, 64, 16,
+                                     8, 16, 0.088, p, p, p, 4096, None)
+    assert st == 2
+    assert cpa.cpa_cascade_verify_shared_workspace_size(4, 3, 2, 3, 8, 2, 128, 16) == 0
+    assert cpa.cpa_cascade_verify_shared_workspace_size(4, 0, 2, 3, 8, 2, 128, 16) == 0
+
+
 def test_tree_shape_checks_before_any_launch(L):
     """Non-null dummy pointers that are never dereferenced: every call fails its host checks."""
     buf = (ctypes.c_uint8 * 4352)()
