@@ -41,6 +41,9 @@ __all__ = [
     "random_bfs_tree",
     "chain_forest",
     "TREE_CONFIGS",
+    "Fp8VerifyWorkload",
+    "make_verify_fp8",
+    "e4m3_codes",
     "SharedWorkload",
     "make_shared_verify",
     "SHARED_CONFIGS",
@@ -406,6 +409,111 @@ def make_tree_verify(B: int, N: int, H_q: int, H_kv: int, head_dim: int = 128,
     if keep_logical:
         wl.prefix_k, wl.prefix_v, wl.tree_k, wl.tree_v = pk, pv, tk, tv
     return wl
+
+
+def e4m3_codes(rng: np.random.Generator, shape, exp_lo: int = 5, exp_hi: int = 8) -> np.ndarray:
+    """Random FP8 E4M3 codes with magnitudes of order one.
+
+    Codes are drawn field by field, with no arithmetic on values: a random
+    sign bit, an exponent field uniform in [exp_lo, exp_hi] (bias 7, so about
+    0.25 to 3.75 for the defaults) and a uniform 3-bit mantissa.  A few codes
+    are replaced by zero and by subnormals so that those encodings appear too.
+    """
+    n = int(np.prod(shape))
+    sign = rng.integers(0, 2, size=n, dtype=np.uint8) << np.uint8(7)
+    expo = rng.integers(exp_lo, exp_hi + 1, size=n, dtype=np.uint8) << np.uint8(3)
+    mant = rng.integers(0, 8, size=n, dtype=np.uint8)
+    codes = sign | expo | mant
+    special = rng.random(n) < 0.01
+    codes[special] = sign[special] | mant[special]  # exponent field 0: zero or subnormal
+    return codes.reshape(shape)
+
+
+@dataclasses.dataclass
+class Fp8VerifyWorkload:
+    """A verify workload whose K/V pools hold FP8 E4M3 codes with scales."""
+
+    B: int
+    topk: int
+    S: int
+    H_q: int
+    H_kv: int
+    head_dim: int
+    page_size: int
+    prefix_lens: np.ndarray
+    q: np.ndarray                    # uint16 bf16 bits [B*topk*S, H_q, d]
+    k_pages: np.ndarray              # uint8 E4M3 codes [num_pages, P, H_kv, d]
+    v_pages: np.ndarray
+    k_scale: np.ndarray              # float32 [1] or [H_kv, d]
+    v_scale: np.ndarray
+    prefix_page_table: np.ndarray
+    draft_page_table: np.ndarray
+    max_prefix_len: int
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_pages.shape[0])
+
+    @property
+    def n_tokens(self) -> int:
+        return self.B * self.topk * self.S
+
+    def unique_kv_tokens(self) -> int:
+        return int(self.prefix_lens.astype(np.int64).sum()) + self.B * self.topk * self.S
+
+    def kv_bytes_per_token(self) -> int:
+        return 2 * self.H_kv * self.head_dim
+
+
+def make_verify_fp8(B: int, topk: int, S: int, H_q: int, H_kv: int, head_dim: int = 128,
+                    page_size: int = 16, L: Optional[int] = None, prefix_lens=None,
+                    scales: str = "tensor", seed: int = 0,
+                    perm_seed: Optional[int] = None) -> Fp8VerifyWorkload:
+    """Build a verify workload over FP8 pools.
+
+    ``scales``: ``"tensor"`` (one random K and one random V scale), ``"channel"``
+    (one per KV head and channel), ``"unit"`` (both 1.0) or ``"pow2"`` (per
+    channel, random powers of two).  Unused page slots hold random codes.
+    """
+    rng = np.random.default_rng(seed)
+    if prefix_lens is not None:
+        lens = np.asarray(prefix_lens, dtype=np.int32).copy()
+    else:
+        lens = np.full(B, L, dtype=np.int32)
+    P, d = page_size, head_dim
+    q = _normal_bf16(rng, (B * topk * S, H_q, d))
+    seqs = [int(x) for x in lens] + [S] * (B * topk)
+    counts = [(n + P - 1) // P for n in seqs]
+    perm_rng = np.random.default_rng(seed * 7919 + 17 if perm_seed is None else perm_seed)
+    perm = perm_rng.permutation(int(sum(counts))).astype(np.int32)
+    k_pages = e4m3_codes(rng, (int(sum(counts)), P, H_kv, d))
+    v_pages = e4m3_codes(rng, (int(sum(counts)), P, H_kv, d))
+    tables, cur = [], 0
+    for n in counts:
+        tables.append(perm[cur:cur + n].copy())
+        cur += n
+    if scales == "tensor":
+        k_scale = rng.uniform(0.25, 2.0, size=1).astype(np.float32)
+        v_scale = rng.uniform(0.25, 2.0, size=1).astype(np.float32)
+    elif scales == "channel":
+        k_scale = rng.uniform(0.25, 2.0, size=(H_kv, d)).astype(np.float32)
+        v_scale = rng.uniform(0.25, 2.0, size=(H_kv, d)).astype(np.float32)
+    elif scales == "unit":
+        k_scale = np.ones(1, np.float32)
+        v_scale = np.ones(1, np.float32)
+    elif scales == "pow2":
+        k_scale = np.exp2(rng.integers(-2, 2, size=(H_kv, d))).astype(np.float32)
+        v_scale = np.exp2(rng.integers(-2, 2, size=(H_kv, d))).astype(np.float32)
+    else:
+        raise ValueError(scales)
+    max_prefix_len = int(lens.max()) if B > 0 else 0
+    return Fp8VerifyWorkload(B=B, topk=topk, S=S, H_q=H_q, H_kv=H_kv, head_dim=d, page_size=P,
+                             prefix_lens=lens, q=q, k_pages=k_pages, v_pages=v_pages,
+                             k_scale=k_scale, v_scale=v_scale,
+                             prefix_page_table=table_matrix(tables[:B],
+                                                            (max_prefix_len + P - 1) // P),
+                             draft_page_table=table_matrix(tables[B:], (S + P - 1) // P),
+                             max_prefix_len=max_prefix_len)
 
 
 @dataclasses.dataclass

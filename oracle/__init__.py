@@ -22,6 +22,10 @@ What is computed, and from which passage:
   shared prefix, all of its request's own prefix and drafts 0..s of branch k;
   ``part`` picks one piece (``"shared"``, ``"own"``, ``"draft"``), both
   prefixes (``"prefix"``) or everything.
+* ``verify_fp8``: verify over FP8 KV pools (KV-cache tutorial, section 4.5,
+  "FP8 KV", per-tensor or per-channel scale): each K/V element is its E4M3
+  code decoded exactly (``e4m3_decode``, from the format definition) times
+  its scale; the attention is then the definition above.
 * ``ancestor_masks``: the tree-attention mask of the KV-cache tutorial
   (section 8.2 tip box; interview question Q14): tree nodes flattened in BFS
   order, A(i) = the ancestors of node i with i itself, M[i, j] = 1 iff j is in
@@ -78,6 +82,11 @@ def _load():
         lib.oracle_verify_shared.argtypes = [P, P, P, i64, P, i32, i32, i32, P, i32, P, i32, P,
                                              i32, i32, i32, i32, i32, i32, i32, i32, f64, P, i64,
                                              P, P, i32]
+        lib.oracle_verify_fp8.restype = i32
+        lib.oracle_verify_fp8.argtypes = [P, P, P, P, P, i32, i64, P, i32, P, i32, P, i32, i32,
+                                          i32, i32, i32, i32, i32, i32, f64, P, i64, P, P, i32]
+        lib.oracle_e4m3_decode.restype = None
+        lib.oracle_e4m3_decode.argtypes = [P, i64, P]
         lib.oracle_merge_state.restype = None
         lib.oracle_merge_state.argtypes = [P, P, P, P, i64, i32, P, P]
         _lib = lib
@@ -182,6 +191,57 @@ def verify_shared_wl(wl, part: str = "full", rows=None, threads: int = 0):
     return verify_shared(wl.q, wl.k_pages, wl.v_pages, wl.shared_page_table, wl.shared_len,
                          wl.prefix_page_table, wl.draft_page_table, wl.prefix_lens, wl.topk,
                          wl.S, wl.H_q, wl.H_kv, part=part, rows=rows, threads=threads)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Exact values (float64) of FP8 E4M3 codes (uint8); NaN for the NaN codes."""
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.zeros(c.shape, dtype=np.float64)
+    lib.oracle_e4m3_decode(_ptr(c), int(c.size), _ptr(out))
+    return out
+
+
+def verify_fp8(q, k_codes, v_codes, k_scale, v_scale, prefix_page_table, draft_page_table,
+               prefix_lens, topk: int, S: int, H_q: int, H_kv: int,
+               scale: Optional[float] = None, part: str = "full",
+               rows: Optional[Sequence[int]] = None, threads: int = 0):
+    """fp64 verify over E4M3 K/V pools; ``k_scale`` / ``v_scale`` hold 1 value or [H_kv, d]."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    kc = np.ascontiguousarray(k_codes, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float64).reshape(-1)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float64).reshape(-1)
+    d = int(q.shape[-1])
+    if ks.size != vs.size or ks.size not in (1, H_kv * d):
+        raise ValueError("scales must hold 1 or H_kv * d values")
+    ppt = np.ascontiguousarray(prefix_page_table, dtype=np.int32)
+    dpt = np.ascontiguousarray(draft_page_table, dtype=np.int32)
+    lens = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+    B = int(lens.shape[0])
+    P = int(kc.shape[1])
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    r, rp, nr = _rows_arg(rows)
+    n = nr if r is not None else B * topk * S * H_q
+    o = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    err = lib.oracle_verify_fp8(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+                                int(ks.size > 1), int(kc.shape[0]), _ptr(ppt), int(ppt.shape[1]),
+                                _ptr(dpt), int(dpt.shape[1]), _ptr(lens), B, topk, S, H_q, H_kv,
+                                d, P, PART_CODES[part], float(scale), rp, nr, _ptr(o), _ptr(lse),
+                                threads)
+    if err:
+        raise ValueError(f"oracle_verify_fp8: {_ERR.get(err, err)}")
+    return o, lse
+
+
+def verify_fp8_wl(wl, part: str = "full", rows=None, threads: int = 0):
+    """``verify_fp8`` on a ``cpa_synth.make_verify_fp8`` workload."""
+    return verify_fp8(wl.q, wl.k_pages, wl.v_pages, wl.k_scale, wl.v_scale,
+                      wl.prefix_page_table, wl.draft_page_table, wl.prefix_lens, wl.topk, wl.S,
+                      wl.H_q, wl.H_kv, part=part, rows=rows, threads=threads)
 
 
 def ancestor_masks(parents) -> np.ndarray:

@@ -66,14 +66,53 @@ static double bf16_bits_to_double(uint16_t b) {
 }
 
 /*
+ * FP8 E4M3 code to double, from the format's definition (1 sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds the
+ * subnormals m/8 * 2^-6; the all-ones exponent with all-ones mantissa is NaN,
+ * and there is no infinity).
+ */
+static double e4m3_to_double(uint8_t b) {
+    int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);          /* (m/8) * 2^(1-7) */
+    else
+        v = ldexp(8.0 + (double)m, e - 10); /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/*
+ * Where a K or V element comes from: the bf16 pools, or FP8 E4M3 pools whose
+ * value is code * scale, with one scale per tensor or one per (KV head,
+ * channel) ("FP8 KV", per-tensor / per-channel: KV-cache tutorial, section
+ * 4.5).
+ */
+typedef struct {
+    const uint16_t *k16, *v16;        /* bf16 bit patterns, or NULL */
+    const uint8_t *k8, *v8;           /* E4M3 codes, or NULL */
+    const double *k_scale, *v_scale;  /* E4M3 only */
+    int per_channel;                  /* scales indexed [kv_head * d + c], else [0] */
+} kv_src_t;
+
+static double kv_elem(const kv_src_t *kv, int is_v, int64_t off, int kv_head, int d, int c) {
+    if (kv->k8) {
+        const uint8_t *pool = is_v ? kv->v8 : kv->k8;
+        const double *sc = is_v ? kv->v_scale : kv->k_scale;
+        double scale = kv->per_channel ? sc[(int64_t)kv_head * d + c] : sc[0];
+        return e4m3_to_double(pool[off + c]) * scale;
+    }
+    return bf16_bits_to_double((is_v ? kv->v16 : kv->k16)[off + c]);
+}
+
+/*
  * Full attention of one query over an explicit list of key rows.
- * key_off[j] is the element offset of key j's head row inside k_pages /
- * v_pages.  Scores, max, sum and weighted sum are taken in that order, as the
+ * key_off[j] is the element offset of key j's head row inside the K / V
+ * pools.  Scores, max, sum and weighted sum are taken in that order, as the
  * softmax definition reads; nothing is blocked or rescaled on the way.
  */
-static void attend_one(const double *q, const uint16_t *k_pages, const uint16_t *v_pages,
-                       const int64_t *key_off, int n_keys, int d, double scale,
-                       double *scores, double *o, double *lse) {
+static void attend_one(const double *q, const kv_src_t *kv, int kv_head, const int64_t *key_off,
+                       int n_keys, int d, double scale, double *scores, double *o, double *lse) {
     for (int c = 0; c < d; ++c) o[c] = 0.0;
     if (n_keys == 0) {
         *lse = -INFINITY;
@@ -81,9 +120,8 @@ static void attend_one(const double *q, const uint16_t *k_pages, const uint16_t 
     }
     double m = -INFINITY;
     for (int j = 0; j < n_keys; ++j) {
-        const uint16_t *kr = k_pages + key_off[j];
         double dot = 0.0;
-        for (int c = 0; c < d; ++c) dot += q[c] * bf16_bits_to_double(kr[c]);
+        for (int c = 0; c < d; ++c) dot += q[c] * kv_elem(kv, 0, key_off[j], kv_head, d, c);
         scores[j] = dot * scale;
         if (scores[j] > m) m = scores[j];
     }
@@ -94,9 +132,8 @@ static void attend_one(const double *q, const uint16_t *k_pages, const uint16_t 
         z += w;
     }
     for (int j = 0; j < n_keys; ++j) {
-        const uint16_t *vr = v_pages + key_off[j];
         double w = scores[j] / z;
-        for (int c = 0; c < d; ++c) o[c] += w * bf16_bits_to_double(vr[c]);
+        for (int c = 0; c < d; ++c) o[c] += w * kv_elem(kv, 1, key_off[j], kv_head, d, c);
     }
     *lse = m + log(z);
 }
@@ -114,6 +151,7 @@ typedef struct {
     int kind;
     int part;
     const uint16_t *q, *k_pages, *v_pages;
+    kv_src_t kv;  /* filled from k_pages / v_pages unless the pools are FP8 */
     int64_t num_pages;
     int H_q, H_kv, d, P;
     double scale;
@@ -232,14 +270,18 @@ static void *worker(void *arg) {
             p->error = ORACLE_BAD_PAGE;
             continue;
         }
-        attend_one(qd, p->k_pages, p->v_pages, key_off, n, d, p->scale, scores, p->o + r * d,
-                   p->lse + r);
+        attend_one(qd, &p->kv, head / (p->H_q / p->H_kv), key_off, n, d, p->scale, scores,
+                   p->o + r * d, p->lse + r);
     }
     free(key_off); free(scores); free(qd);
     return NULL;
 }
 
 static int run_rows(problem_t *p, int n_threads) {
+    if (!p->kv.k8) {
+        p->kv.k16 = p->k_pages;
+        p->kv.v16 = p->v_pages;
+    }
     if (n_threads <= 0) {
         long c = sysconf(_SC_NPROCESSORS_ONLN);
         n_threads = c > 0 ? (int)c : 1;
@@ -301,6 +343,56 @@ int oracle_verify(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_
     p.max_keys = maxL + S;
     p.o = o; p.lse = lse;
     return run_rows(&p, n_threads);
+}
+
+/*
+ * Verify over FP8 KV pools ("FP8 KV" of the KV-cache tutorial, section 4.5:
+ * per-tensor or per-channel FP8).  k_codes / v_codes are E4M3 codes laid out
+ * like the bf16 pools, [num_pages, P, H_kv, d]; element value = decoded code *
+ * scale, with k_scale / v_scale of length 1 (per_channel = 0) or H_kv * d
+ * (per_channel = 1, index kv_head * d + channel).  Everything else as
+ * oracle_verify.
+ */
+int oracle_verify_fp8(const uint16_t *q, const uint8_t *k_codes, const uint8_t *v_codes,
+                      const double *k_scale, const double *v_scale, int per_channel,
+                      int64_t num_pages, const int32_t *prefix_pt, int prefix_stride,
+                      const int32_t *draft_pt, int draft_stride, const int32_t *prefix_lens,
+                      int B, int topk, int S, int H_q, int H_kv, int d, int P, int part,
+                      double scale, const int64_t *rows, int64_t n_rows, double *o, double *lse,
+                      int n_threads) {
+    if (B < 0 || topk < 1 || S < 1 || H_kv < 1 || H_q % H_kv != 0 || d < 1 || P < 1 ||
+        part < 0 || part > 2 || !k_codes || !v_codes || !k_scale || !v_scale)
+        return ORACLE_BAD_ARG;
+    problem_t p;
+    memset(&p, 0, sizeof p);
+    p.kind = KIND_VERIFY;
+    p.part = part;
+    p.q = q; p.num_pages = num_pages;
+    p.kv.k8 = k_codes; p.kv.v8 = v_codes;
+    p.kv.k_scale = k_scale; p.kv.v_scale = v_scale; p.kv.per_channel = per_channel ? 1 : 0;
+    p.H_q = H_q; p.H_kv = H_kv; p.d = d; p.P = P; p.scale = scale;
+    p.prefix_pt = prefix_pt; p.draft_pt = draft_pt; p.prefix_lens = prefix_lens;
+    p.prefix_stride = prefix_stride; p.draft_stride = draft_stride;
+    p.B = B; p.topk = topk; p.S = S;
+    int64_t total_rows = (int64_t)B * topk * S * H_q;
+    p.rows = rows;
+    p.n_rows = rows ? n_rows : total_rows;
+    int maxL = 0;
+    for (int b = 0; b < B; ++b) {
+        if (prefix_lens[b] < 0) return ORACLE_BAD_ARG;
+        if (prefix_lens[b] > maxL) maxL = prefix_lens[b];
+    }
+    if (rows)
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (rows[r] < 0 || rows[r] >= total_rows) return ORACLE_BAD_ARG;
+    p.max_keys = maxL + S;
+    p.o = o; p.lse = lse;
+    return run_rows(&p, n_threads);
+}
+
+/* Decode n E4M3 codes to doubles (for checking the decoder). */
+void oracle_e4m3_decode(const uint8_t *codes, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_to_double(codes[i]);
 }
 
 /*
