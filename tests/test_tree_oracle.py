@@ -9,7 +9,9 @@ force on logical (de-paged) data, and the two special cases that reduce to
 functions pinned elsewhere (a forest of chains is chain-per-branch verify; a
 single chain is prefix-hit prefill).
 """
+import json
 import math
+import os
 
 import numpy as np
 import pytest
@@ -38,6 +40,19 @@ def _bits_to_sets(masks, N):
 def test_ancestor_masks_hand_drawn_tree():
     got = _bits_to_sets(oracle.ancestor_masks(HAND_PARENTS), len(HAND_PARENTS))
     assert got == HAND_ANCESTORS
+
+
+def test_branch_example_of_the_pages_as_a_forest():
+    """The cascade page's 4 branches of 3 drafts, flattened in BFS order, give its visible sets."""
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "branch_visibility.json")))
+    topk, S = g["topk"], g["S"]
+    masks = oracle.ancestor_masks(cpa_synth.chain_forest(topk, S))
+    node = lambda k, j: j * topk + k  # BFS: level j holds draft j of every branch
+    for k in range(topk):
+        for j in range(S):
+            want = {node(kk, jj) for kk, jj in g["visible_drafts"][f"d_{k}{j}"]}
+            assert _bits_to_sets([masks[node(k, j)]], topk * S)[0] == want
 
 
 def test_ancestor_masks_of_a_chain_are_causal():
