@@ -56,8 +56,11 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 
 // Timestamps of pipeline events for a few CTAs, only in builds that define
 // CPA_TRACE (a diagnostic build provides the buffer); otherwise no code.
+// Buffer: [4 CTAs][64 events][1024] clock64 stamps, then every CTA's start and
+// end %globaltimer at kTraceCtaBase + 2 * CTA (+ 0 start, + 1 end).
 #ifdef CPA_TRACE
 static __device__ unsigned long long* cpa_trace_buf = nullptr;
+constexpr int kTraceCtaBase = 4 * 64 * 1024;
 #define CPA_TRACE_EVENT(ev, idx)                                                  \
     do {                                                                          \
         if (cpa_trace_local && blockIdx.x < 4 && (idx) < 1024)                    \
@@ -532,9 +535,12 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     tc_fence_after_sync();
     schedule(p, ctrl);
 #ifdef CPA_TRACE
-    if (threadIdx.x == 0 && cpa_trace_local && blockIdx.x < 4) {
-        cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1000] = clock64();
-        cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1001] = globaltimer_ns();
+    if (threadIdx.x == 0 && cpa_trace_local) {
+        if (blockIdx.x < 4) {
+            cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1000] = clock64();
+            cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1001] = globaltimer_ns();
+        }
+        cpa_trace_local[kTraceCtaBase + 2 * blockIdx.x] = globaltimer_ns();
     }
 #endif
     const uint32_t tmem = ctrl->tmem_base;
@@ -1418,9 +1424,12 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
 #ifdef CPA_TRACE
-    if (threadIdx.x == 0 && cpa_trace_local && blockIdx.x < 4) {
-        cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1002] = clock64();
-        cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1003] = globaltimer_ns();
+    if (threadIdx.x == 0 && cpa_trace_local) {
+        if (blockIdx.x < 4) {
+            cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1002] = clock64();
+            cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1003] = globaltimer_ns();
+        }
+        cpa_trace_local[kTraceCtaBase + 2 * blockIdx.x + 1] = globaltimer_ns();
     }
 #endif
     if (warp == 1) {
