@@ -73,3 +73,43 @@ def test_nan_padding_only_outside_sequences():
             pos = ((L - 1) // P) * P + slot
             is_nan = np.all(wl.k_pages[last, slot] == 0x7FC0)
             assert is_nan == (pos >= L)
+
+
+def test_tree_workload_layout():
+    wl = cpa_synth.make_tree_verify(B=3, N=11, H_q=4, H_kv=2, head_dim=8, page_size=4,
+                                    prefix_lens=[7, 0, 12], n_roots=2, seed=4, keep_logical=True)
+    assert wl.q.shape == (3 * 11, 4, 8) and wl.parents.shape == (3, 11)
+    assert wl.tree_page_table.shape == (3, 3)
+    used = []
+    for b in range(3):
+        n = (int(wl.prefix_lens[b]) + 3) // 4
+        used += wl.prefix_page_table[b, :n].tolist() + wl.tree_page_table[b].tolist()
+        # every parent precedes its child; exactly n_roots roots
+        par = wl.parents[b]
+        assert (par[par >= 0] < np.nonzero(par >= 0)[0]).all()
+        assert int((par == -1).sum()) == 2
+        for j in range(11):
+            page = wl.tree_page_table[b, j // 4]
+            assert np.array_equal(wl.k_pages[page, j % 4], wl.tree_k[b][j])
+    assert len(used) == len(set(used)) == wl.num_pages
+
+
+def test_shared_workload_layout():
+    wl = cpa_synth.make_shared_verify(B=4, n_groups=2, shared_len=9, topk=2, S=3, H_q=4, H_kv=2,
+                                      head_dim=8, page_size=4, prefix_lens=[5, 0, 8, 1], seed=5,
+                                      keep_logical=True)
+    assert wl.shared_page_table.shape == (2, 3)
+    for g in range(2):
+        for pos in range(9):
+            page = wl.shared_page_table[g, pos // 4]
+            assert np.array_equal(wl.v_pages[page, pos % 4], wl.shared_v[g][pos])
+    assert wl.unique_kv_tokens() == 2 * 9 + 14 + 4 * 2 * 3
+
+
+def test_fp8_codes_have_no_nan_and_order_one_magnitudes():
+    rng = np.random.default_rng(0)
+    c = cpa_synth.e4m3_codes(rng, (4096,))
+    assert not np.any((c & 0x7F) == 0x7F)
+    expo = (c >> 3) & 0xF
+    assert set(np.unique(expo).tolist()) <= {0, 5, 6, 7, 8}
+    assert (expo == 0).mean() < 0.05
