@@ -58,6 +58,15 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_bf16_tflops():
+    """Burst bf16 dense peak (a kernel timed alone), measured if recorded."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1900.0
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
 
@@ -199,6 +208,169 @@ def run_reference(args, world, rank):
     return 0
 
 
+def pct(xs, q):
+    return float(np.percentile(np.asarray(xs, dtype=np.float64), q))
+
+
+def launch_stats(per_ms):
+    """Per-launch CUDA-event times (ms) -> mean / median / p10 / p90 in us."""
+    return {"mean": 1e3 * float(np.mean(per_ms)), "median": 1e3 * pct(per_ms, 50),
+            "p10": 1e3 * pct(per_ms, 10), "p90": 1e3 * pct(per_ms, 90), "n": len(per_ms)}
+
+
+class Timer:
+    """CUDA-event timing on one stream, with an optional L2 flush before every call."""
+
+    def __init__(self, torch, stream, flush_bytes: int):
+        self.torch = torch
+        self.stream = stream
+        # writing a buffer twice the size of L2 evicts every line a call could reuse
+        self.flush_buf = torch.empty(flush_bytes, dtype=torch.uint8, device=stream.device)
+
+    def flush(self):
+        self.flush_buf.fill_(1)
+
+    def back_to_back(self, fn, steps, warmup, barrier=lambda: None):
+        """`steps` calls back to back: (total ms, per-call ms)."""
+        torch = self.torch
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        evs[0].record(self.stream)
+        for i in range(steps):
+            fn()
+            evs[i + 1].record(self.stream)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+        return evs[0].elapsed_time(evs[-1]), per
+
+    def cold(self, fn, iters, warmup=3):
+        """Per-call ms of `iters` calls, each after an L2 flush (flush not timed)."""
+        torch = self.torch
+        for _ in range(warmup):
+            fn()
+        per = []
+        for _ in range(iters):
+            self.flush()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(self.stream)
+            fn()
+            b.record(self.stream)
+            b.synchronize()
+            per.append(a.elapsed_time(b))
+        return per
+
+
+def to_device(torch, dev, a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return (t.view(dtype) if dtype is not None else t).to(dev)
+
+
+def verify_config_row(torch, cpa, cpa_synth, timer, dev, name, peak, iters, cpu, rows_budget):
+    """Cascade and naive expand on one verify workload (cold L2), and the oracle beside them."""
+    wl = cpa_synth.make_verify(**cpa_synth.VERIFY_CONFIGS[name])
+    q = to_device(torch, dev, wl.q, torch.bfloat16)
+    kp = to_device(torch, dev, wl.k_pages, torch.bfloat16)
+    vp = to_device(torch, dev, wl.v_pages, torch.bfloat16)
+    ppt, dpt, lens = (to_device(torch, dev, a) for a in (wl.prefix_page_table,
+                                                         wl.draft_page_table, wl.prefix_lens))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[0], wl.H_q, dtype=torch.float32, device=dev)
+    mpl = wl.max_prefix_len
+
+    def cascade():
+        cpa.cpa_cascade_verify(q, kp, vp, ppt, dpt, lens, wl.topk, wl.S, max_prefix_len=mpl,
+                               o=o, lse=lse)
+
+    def naive():
+        cpa.cpa_naive_expand_verify(q, kp, vp, ppt, dpt, lens, wl.topk, wl.S,
+                                    max_prefix_len=mpl, o=o, lse=lse)
+
+    unique = wl.unique_kv_tokens() * wl.kv_bytes_per_token()
+    c = launch_stats(timer.cold(cascade, iters))
+    n = launch_stats(timer.cold(naive, max(5, iters // 4)))
+    row = {
+        "config": name, "unique_kv_bytes": unique,
+        "naive_kv_bytes": wl.naive_kv_tokens() * wl.kv_bytes_per_token(),
+        "cascade_us": c, "naive_us": n,
+        "cascade_gbs": unique / (c["median"] * 1e-6) / 1e9,
+        "frac_of_hbm_peak": unique / (c["median"] * 1e-6) / 1e9 / peak,
+        "speedup_cascade_vs_naive": n["median"] / c["median"],
+    }
+    del q, kp, vp
+    torch.cuda.empty_cache()
+    if cpu:
+        import oracle
+
+        n_rows = wl.n_tokens * wl.H_q
+        rows = np.arange(min(n_rows, rows_budget), dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.verify_wl(wl, rows=rows)
+        dt = time.perf_counter() - t0
+        # unique KV bytes scaled by the share of (row, key) pairs the sample covered
+        keys = (wl.prefix_lens.astype(np.int64) + wl.S).repeat(wl.topk * wl.S * wl.H_q)
+        share = float(keys[:len(rows)].sum()) / float(keys.sum())
+        row["oracle"] = {"value": unique * share / dt / 1e9, "unit": "GB/s",
+                         "cores": os.cpu_count() or 1, "kind": "oracle", "seconds": dt,
+                         "sample": f"first {len(rows)} of {n_rows} (token, head) rows"}
+    return row
+
+
+def prefill_rows(torch, cpa, cpa_synth, timer, dev, peak_tf, iters, cpu):
+    """Prefix-hit prefill (B=8, N=8192) at h = 0, 0.5, 0.75: time, TFLOP/s of visible
+    pairs, T(h)/T(0) beside 1 - h^2, and the oracle on sampled rows."""
+    c = dict(cpa_synth.PREFILL_CONFIG)
+    hits = c.pop("hits")
+    out, t_zero = [], None
+    for h in hits:
+        H = int(h * c["N"])
+        wl = cpa_synth.make_prefill(H=H, **c)
+        q = to_device(torch, dev, wl.q, torch.bfloat16)
+        kp = to_device(torch, dev, wl.k_pages, torch.bfloat16)
+        vp = to_device(torch, dev, wl.v_pages, torch.bfloat16)
+        pt = to_device(torch, dev, wl.page_table)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[0], wl.H_q, dtype=torch.float32, device=dev)
+
+        def call():
+            cpa.cpa_prefill_hit(q, kp, vp, pt, wl.B, wl.N, wl.H, o=o, lse=lse)
+
+        st = launch_stats(timer.cold(call, iters))
+        flops = 4.0 * wl.head_dim * wl.H_q * wl.B * wl.visible_pairs()
+        tf = flops / (st["median"] * 1e-6) / 1e12
+        if t_zero is None:
+            t_zero = st["median"]
+        row = {"config": f"prefill_hit h={h}", "B": wl.B, "N": wl.N, "H": wl.H,
+               "us": st, "flops": flops, "tflops": tf, "frac_of_bf16_peak": tf / peak_tf,
+               "t_over_t0": st["median"] / t_zero,
+               "pair_ratio": 1.0 - (wl.H * (wl.H + 1)) / (wl.N * (wl.N + 1))}
+        del q, kp, vp
+        torch.cuda.empty_cache()
+        if cpu:
+            import oracle
+
+            M = wl.N - wl.H
+            rng = np.random.default_rng(7)
+            toks = np.sort(rng.choice(wl.B * M, size=64, replace=False))
+            rows = (toks[:, None] * wl.H_q + np.arange(wl.H_q)[None, :]).reshape(-1)
+            t0 = time.perf_counter()
+            oracle.prefill_wl(wl, rows=rows)
+            dt = time.perf_counter() - t0
+            keys = float(sum(wl.H + (int(t) % M) + 1 for t in toks) * wl.H_q)
+            row["oracle"] = {"value": 4.0 * wl.head_dim * keys / dt / 1e12, "unit": "TFLOP/s",
+                             "cores": os.cpu_count() or 1, "kind": "oracle", "seconds": dt,
+                             "sample": f"64 random suffix tokens x all {wl.H_q} heads",
+                             "extrapolated_full_s": dt * flops / (4.0 * wl.head_dim * keys)}
+        out.append(row)
+    return out
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -239,6 +411,7 @@ def run_ours(args, world, rank, local):
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     mpl = wl.max_prefix_len
+    timer = Timer(torch, stream, 2 * L2_BYTES)
 
     def cascade():
         cpa.cpa_cascade_verify(q, kp, vp, ppt, dpt, lens, topk, S, max_prefix_len=mpl, o=o,
@@ -258,62 +431,56 @@ def run_ours(args, world, rank, local):
     def max_over_ranks(x: float) -> float:
         return reduce_max(x, pg, dev)
 
-    def timed(fn, steps, per_launch=False):
-        """Time `steps` calls: total ms (events around the whole run) and per-call ms."""
-        for _ in range(args.warmup):
-            fn()
-        torch.cuda.synchronize()
-        barrier()
-        torch.cuda.synchronize()
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-        evs[0].record(stream)
-        for i in range(steps):
-            fn()
-            evs[i + 1].record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        torch.cuda.synchronize()
-        per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
-        return evs[0].elapsed_time(evs[-1]), per
-
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    total_ms, per_ms = timed(cascade, args.steps)
+    total_ms, per_ms = timer.back_to_back(cascade, args.steps, args.warmup, barrier)
     clock_info = clocks.stop()
     total_ms = max_over_ranks(total_ms)
     ms_per_step = total_ms / args.steps
     value = weak_scaling_gbs(unique_bytes, world, args.steps, total_ms)
-    launch_ms = statistics.mean(per_ms)
+    ls = launch_stats(per_ms)
+    launch_ms = ls["mean"] * 1e-3
     achieved = unique_bytes / (launch_ms * 1e-3) / 1e9
 
-    naive_total, _ = timed(naive, args.steps)
+    naive_total, _ = timer.back_to_back(naive, args.steps, args.warmup, barrier)
     naive_total = max_over_ranks(naive_total)
     naive_ms = naive_total / args.steps
 
-    # end to end through the public API: host inputs -> device, call, result -> host
+    # the same call with L2 flushed before every launch (cold-L2 figure)
+    cold = launch_stats(timer.cold(cascade, args.cold_iters))
+    cold_naive = launch_stats(timer.cold(naive, max(5, args.cold_iters // 4)))
+
+    # end to end through the public API: host inputs -> device, call, result -> host.
+    # The two KV pools go up on two streams at once (one copy stream does not fill
+    # the host link); the call waits for both.
     h_o = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
     h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_ppt, h_dpt, h_lens))
     d2h = h_o.numel() * 2 + h_lse.numel() * 4
+    side = torch.cuda.Stream(dev)
 
     def e2e_step():
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            vp.copy_(h_v, non_blocking=True)
         q.copy_(h_q, non_blocking=True)
         kp.copy_(h_k, non_blocking=True)
-        vp.copy_(h_v, non_blocking=True)
         ppt.copy_(h_ppt, non_blocking=True)
         dpt.copy_(h_dpt, non_blocking=True)
         lens.copy_(h_lens, non_blocking=True)
+        stream.wait_stream(side)
         cascade()
         h_o.copy_(o, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 10))
-    e2e_total, _ = timed(e2e_step, e2e_steps)
+    e2e_total, _ = timer.back_to_back(e2e_step, e2e_steps, args.warmup, barrier)
     e2e_total = max_over_ranks(e2e_total)
     e2e_value = weak_scaling_gbs(unique_bytes, world, e2e_steps, e2e_total)
 
     peak, peak_kind = measured_peaks()
+    peak_tf = measured_bf16_tflops()
     traffic = None
     if os.path.exists(PROFILE_SUMMARY):
         with open(PROFILE_SUMMARY) as f:
@@ -321,8 +488,17 @@ def run_ours(args, world, rank, local):
         if prof.get("kernel_hash") == kernel_hash():
             traffic = prof.get("dram_bytes_per_launch")
 
+    do_cpu = rank == 0 and not args.no_cpu_baseline
+    configs = []
+    if rank == 0 and args.configs == "all":
+        for name in ("llama3_8b", "long_variable"):
+            configs.append(verify_config_row(torch, cpa, cpa_synth, timer, dev, name, peak,
+                                             args.cold_iters, do_cpu, rows_budget=4096))
+        configs.extend(prefill_rows(torch, cpa, cpa_synth, timer, dev, peak_tf,
+                                    max(5, args.cold_iters // 10), do_cpu))
+
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if do_cpu:
         import oracle.build
 
         oracle.build.build()
@@ -339,7 +515,8 @@ def run_ours(args, world, rank, local):
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "per_gpu_batch": B,
                        "l2": f"inputs larger than L2 (KV pool {kp.numel() * 2 * 2 / 2**20:.0f} MiB"
-                             f" vs {L2_BYTES // 2**20} MiB L2), no flush"},
+                             f" vs {L2_BYTES // 2**20} MiB L2), no flush between the timed "
+                             f"steps; cold_l2 flushes L2 before every launch"},
             "us_per_step": ms_per_step * 1e3,
             "naive_expand": {"us_per_step": naive_ms * 1e3,
                              "kv_gbs_unique": unique_bytes / (naive_ms * 1e-3) / 1e9,
@@ -348,7 +525,13 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_kind": peak_kind, "algorithmic_bytes_per_launch": unique_bytes,
-                         "launch_us": launch_ms * 1e3},
+                         "launch_us": ls["mean"], "launch_us_median": ls["median"],
+                         "launch_us_p10": ls["p10"], "launch_us_p90": ls["p90"]},
+            "cold_l2": {"cascade_us": cold, "naive_us": cold_naive,
+                        "cascade_gbs": unique_bytes / (cold["median"] * 1e-6) / 1e9,
+                        "frac": unique_bytes / (cold["median"] * 1e-6) / 1e9 / peak,
+                        "speedup_cascade_vs_naive": cold_naive["median"] / cold["median"]},
+            "configs": configs,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "us_per_step": e2e_total / e2e_steps * 1e3},
@@ -368,6 +551,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", choices=["all", "none"], default="all",
+                    help="also time the other verify configs and the prefill (cold L2)")
+    ap.add_argument("--cold-iters", type=int, default=100,
+                    help="launches timed one by one after an L2 flush")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

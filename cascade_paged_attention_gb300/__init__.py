@@ -5,6 +5,12 @@ and devices, allocates outputs / workspace with PyTorch when the caller does
 not pass them, and calls the C entry point of the same name on PyTorch's
 current CUDA stream.  All arithmetic runs in the library's CUDA kernels; there
 is no fallback path, and a missing library raises ``RuntimeError``.
+
+Every call that takes a workspace (and the static-scratch call) accepts
+``check=True``: after the launch it reads the device status word
+(synchronising the stream) and raises ``CpaError`` when the GPU recorded a bad
+page id, a bad prefix length, a bad tree parent or a pipeline timeout.  The
+outputs of such a call are undefined.
 """
 from __future__ import annotations
 
@@ -37,6 +43,7 @@ __all__ = [
     "cpa_tree_verify",
     "cpa_tree_pass_b",
     "cpa_get_device_status",
+    "cpa_noalloc_device_status",
     "cpa_debug_wait_timeout",
     "cpa_plan_partition",
     "declared_functions",
@@ -73,13 +80,16 @@ def build_library(force: bool = False) -> str:
 
 
 def lib() -> ctypes.CDLL:
+    """The loaded library: libcpa.so, or the build that $CPA_LIBRARY names (the
+    diagnostic trace build)."""
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+    path = os.environ.get("CPA_LIBRARY") or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
                            "`python -m cascade_paged_attention_gb300.build`")
-    L = ctypes.CDLL(LIB_PATH)
+    L = ctypes.CDLL(path)
     P, I, I64, F, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                         ctypes.c_size_t)
     verify_args = [P, P, P, P, I, P, I, P, I, I, I, I, I, I, I, I, I, F, P, P, P, SZ, P]
@@ -105,6 +115,7 @@ def lib() -> ctypes.CDLL:
                                 P]),
         "cpa_tree_pass_b": (I, [P, P, P, P, I, P, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
         "cpa_get_device_status": (I, [P, ctypes.POINTER(ctypes.c_uint32), P]),
+        "cpa_noalloc_device_status": (I, [ctypes.POINTER(ctypes.c_uint32), P]),
         "cpa_debug_wait_timeout": (I, [P, SZ, I, P]),
         "cpa_plan_partition": (I, [I64, I, I, I64, ctypes.POINTER(ctypes.c_int64),
                                    ctypes.POINTER(ctypes.c_int64)]),
@@ -189,6 +200,13 @@ def _check(fn: str, status: int):
         raise CpaError(fn, status)
 
 
+def _check_device(fn: str, workspace: torch.Tensor, stream):
+    """Raise if the device status word of `workspace` has any bit set (synchronises)."""
+    st, word = cpa_get_device_status(workspace, stream)
+    if st != 0:
+        raise CpaError(f"{fn} (device status word {word:#x})", st)
+
+
 def _verify_shapes(q, k_pages, v_pages, prefix_page_table, prefix_lens, topk, S):
     _need(q, "q", torch.bfloat16, 3)
     _need(k_pages, "k_pages", torch.bfloat16, 4)
@@ -206,7 +224,7 @@ def _verify_shapes(q, k_pages, v_pages, prefix_page_table, prefix_lens, topk, S)
 
 
 def _verify_call(name, q, k_pages, v_pages, prefix_page_table, draft_page_table, prefix_lens,
-                 topk, S, max_prefix_len, sm_scale, o, lse, workspace, stream):
+                 topk, S, max_prefix_len, sm_scale, o, lse, workspace, stream, check=False):
     B, H_q, H_kv, d, P, num_pages = _verify_shapes(q, k_pages, v_pages, prefix_page_table,
                                                     prefix_lens, topk, S)
     _need(draft_page_table, "draft_page_table", torch.int32, 2)
@@ -230,6 +248,8 @@ def _verify_call(name, q, k_pages, v_pages, prefix_page_table, draft_page_table,
         _ptr(prefix_lens), B, topk, S, H_q, H_kv, d, P, num_pages, int(max_prefix_len),
         float(sm_scale), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _check(name, st)
+    if check:
+        _check_device(name, ws, stream)
     return o, lse
 
 
@@ -237,17 +257,18 @@ def _verify_call(name, q, k_pages, v_pages, prefix_page_table, draft_page_table,
 def cpa_cascade_verify(q, k_pages, v_pages, prefix_page_table, draft_page_table, prefix_lens,
                        topk: int, S: int, max_prefix_len: Optional[int] = None,
                        sm_scale: Optional[float] = None, o=None, lse=None, workspace=None,
-                       stream=None):
+                       stream=None, check: bool = False):
     """Cascade verify attention (Pass A + Pass B + merge).  Returns (o bf16, lse fp32)."""
     return _verify_call("cpa_cascade_verify", q, k_pages, v_pages, prefix_page_table,
                         draft_page_table, prefix_lens, topk, S, max_prefix_len, sm_scale, o, lse,
-                        workspace, stream)
+                        workspace, stream, check)
 
 
 def cpa_cascade_verify_noalloc(q, k_pages, v_pages, prefix_page_table, draft_page_table,
                                prefix_lens, topk: int, S: int, o, lse,
                                max_prefix_len: Optional[int] = None,
-                               sm_scale: Optional[float] = None, stream=None):
+                               sm_scale: Optional[float] = None, stream=None,
+                               check: bool = False):
     """Cascade verify without a workspace, for callers that cannot allocate device memory.
 
     The library keeps its scratch in a fixed-size array it owns on every GPU,
@@ -272,22 +293,26 @@ def cpa_cascade_verify_noalloc(q, k_pages, v_pages, prefix_page_table, draft_pag
         _ptr(prefix_lens), B, topk, S, H_q, H_kv, d, P, num_pages, int(max_prefix_len),
         float(sm_scale), _ptr(o), _ptr(lse), _stream(stream))
     _check("cpa_cascade_verify_noalloc", st)
+    if check:
+        st, word = cpa_noalloc_device_status(stream)
+        if st != 0:
+            raise CpaError(f"cpa_cascade_verify_noalloc (device status word {word:#x})", st)
     return o, lse
 
 
 def cpa_naive_expand_verify(q, k_pages, v_pages, prefix_page_table, draft_page_table,
                             prefix_lens, topk: int, S: int, max_prefix_len: Optional[int] = None,
                             sm_scale: Optional[float] = None, o=None, lse=None, workspace=None,
-                            stream=None):
+                            stream=None, check: bool = False):
     """Naive-expand verify (the baseline).  Returns (o bf16, lse fp32)."""
     return _verify_call("cpa_naive_expand_verify", q, k_pages, v_pages, prefix_page_table,
                         draft_page_table, prefix_lens, topk, S, max_prefix_len, sm_scale, o, lse,
-                        workspace, stream)
+                        workspace, stream, check)
 
 
 def cpa_cascade_pass_a(q, k_pages, v_pages, prefix_page_table, prefix_lens, topk: int, S: int,
                        max_prefix_len: Optional[int] = None, sm_scale: Optional[float] = None,
-                       o_a=None, lse_a=None, workspace=None, stream=None):
+                       o_a=None, lse_a=None, workspace=None, stream=None, check: bool = False):
     """Pass A alone.  Returns (o_a fp32, lse_a fp32)."""
     B, H_q, H_kv, d, P, num_pages = _verify_shapes(q, k_pages, v_pages, prefix_page_table,
                                                     prefix_lens, topk, S)
@@ -309,12 +334,14 @@ def cpa_cascade_pass_a(q, k_pages, v_pages, prefix_page_table, prefix_lens, topk
         int(max_prefix_len), float(sm_scale), _ptr(o_a), _ptr(lse_a), _ptr(ws), ws.numel(),
         _stream(stream))
     _check("cpa_cascade_pass_a", st)
+    if check:
+        _check_device("cpa_cascade_pass_a", ws, stream)
     return o_a, lse_a
 
 
 def cpa_cascade_pass_b(q, k_pages, v_pages, draft_page_table, B: int, topk: int, S: int,
                        sm_scale: Optional[float] = None, o_b=None, lse_b=None, workspace=None,
-                       stream=None):
+                       stream=None, check: bool = False):
     """Pass B alone (warp-level draft kernel).  Returns (o_b fp32, lse_b fp32)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_pages, "k_pages", torch.bfloat16, 4)
@@ -336,6 +363,8 @@ def cpa_cascade_pass_b(q, k_pages, v_pages, draft_page_table, B: int, topk: int,
         B, topk, S, H_q, H_kv, d, P, num_pages, float(sm_scale), _ptr(o_b), _ptr(lse_b),
         _ptr(ws), ws.numel(), _stream(stream))
     _check("cpa_cascade_pass_b", st)
+    if check:
+        _check_device("cpa_cascade_pass_b", ws, stream)
     return o_b, lse_b
 
 
@@ -360,7 +389,7 @@ def cpa_merge_state(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=Non
 
 def cpa_prefill_hit(q, k_pages, v_pages, page_table, B: int, N: int, H_hit: int,
                     part: int = PREFILL_FULL, sm_scale: Optional[float] = None, o=None, lse=None,
-                    workspace=None, stream=None):
+                    workspace=None, stream=None, check: bool = False):
     """Prefix-hit prefill.  Returns (o, lse); o is bf16 for PREFILL_FULL, fp32 otherwise."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_pages, "k_pages", torch.bfloat16, 4)
@@ -385,6 +414,8 @@ def cpa_prefill_hit(q, k_pages, v_pages, page_table, B: int, N: int, H_hit: int,
         H_hit, H_q, H_kv, d, P, num_pages, float(sm_scale), int(part), _ptr(o), _ptr(lse),
         _ptr(ws), ws.numel(), _stream(stream))
     _check("cpa_prefill_hit", st)
+    if check:
+        _check_device("cpa_prefill_hit", ws, stream)
     return o, lse
 
 
@@ -398,7 +429,7 @@ def cpa_cascade_verify_shared(q, k_pages, v_pages, shared_page_table, shared_len
                               prefix_page_table, draft_page_table, prefix_lens, topk: int, S: int,
                               max_prefix_len: Optional[int] = None,
                               sm_scale: Optional[float] = None, o=None, lse=None, workspace=None,
-                              stream=None):
+                              stream=None, check: bool = False):
     """Multi-level cascade verify.  Returns (o bf16, lse fp32).
 
     ``shared_page_table`` int32 [n_groups, stride]: one shared prefix of
@@ -431,6 +462,8 @@ def cpa_cascade_verify_shared(q, k_pages, v_pages, shared_page_table, shared_len
         _ptr(prefix_lens), B, topk, S, H_q, H_kv, d, P, num_pages, int(max_prefix_len),
         float(sm_scale), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _check("cpa_cascade_verify_shared", st)
+    if check:
+        _check_device("cpa_cascade_verify_shared", ws, stream)
     return o, lse
 
 
@@ -457,7 +490,7 @@ def _tree_shapes(q, k_pages, v_pages, tree_page_table, tree_parents):
 def cpa_tree_verify(q, k_pages, v_pages, prefix_page_table, tree_page_table, prefix_lens,
                     tree_parents, max_prefix_len: Optional[int] = None,
                     sm_scale: Optional[float] = None, o=None, lse=None, workspace=None,
-                    stream=None):
+                    stream=None, check: bool = False):
     """Verify over draft trees (prefix pass + tree pass + merge).  Returns (o bf16, lse fp32).
 
     ``tree_parents`` int32 [B, N]: parent BFS index of each node, -1 for a root.
@@ -487,12 +520,14 @@ def cpa_tree_verify(q, k_pages, v_pages, prefix_page_table, tree_page_table, pre
         int(max_prefix_len), float(sm_scale), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
         _stream(stream))
     _check("cpa_tree_verify", st)
+    if check:
+        _check_device("cpa_tree_verify", ws, stream)
     return o, lse
 
 
 def cpa_tree_pass_b(q, k_pages, v_pages, tree_page_table, tree_parents,
                     sm_scale: Optional[float] = None, o_b=None, lse_b=None, workspace=None,
-                    stream=None):
+                    stream=None, check: bool = False):
     """The tree part alone (each node against its ancestor-or-self nodes).  Returns fp32 (o_b, lse_b)."""
     B, N, H_q, H_kv, d, P, num_pages = _tree_shapes(q, k_pages, v_pages, tree_page_table,
                                                      tree_parents)
@@ -510,6 +545,8 @@ def cpa_tree_pass_b(q, k_pages, v_pages, tree_page_table, tree_parents,
         _ptr(tree_parents), B, N, H_q, H_kv, d, P, num_pages, float(sm_scale), _ptr(o_b),
         _ptr(lse_b), _ptr(ws), ws.numel(), _stream(stream))
     _check("cpa_tree_pass_b", st)
+    if check:
+        _check_device("cpa_tree_pass_b", ws, stream)
     return o_b, lse_b
 
 
@@ -517,6 +554,13 @@ def cpa_get_device_status(workspace: torch.Tensor, stream=None) -> tuple[int, in
     """(status code, raw device status word) of the last call on `workspace` (synchronises)."""
     word = ctypes.c_uint32(0)
     st = lib().cpa_get_device_status(_ptr(workspace), ctypes.byref(word), _stream(stream))
+    return st, word.value
+
+
+def cpa_noalloc_device_status(stream=None) -> tuple[int, int]:
+    """(status code, raw word) of the static scratch of the current device (synchronises)."""
+    word = ctypes.c_uint32(0)
+    st = lib().cpa_noalloc_device_status(ctypes.byref(word), _stream(stream))
     return st, word.value
 
 

@@ -18,6 +18,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcpa.so")
+# Diagnostic variant with the kernels' trace hooks compiled in (-DCPA_TRACE);
+# never loaded unless CPA_LIBRARY names it.
+TRACE_LIB = os.path.join(HERE, "libcpa_trace.so")
 SOURCES = ["cpa_api.cu", "cpa_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -37,26 +40,31 @@ def _inputs():
     return files
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          trace: bool = False) -> str:
+    out = TRACE_LIB if trace else LIB
+    if not force and not _stale(out):
+        return out
+    bdir = os.path.join(BUILD, "trace") if trace else BUILD
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
     common = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
                      "-I", CSRC, "--expt-relaxed-constexpr", "-Xcudafe",
                      "--diag_suppress=177"]
+    if trace:
+        common += ["-DCPA_TRACE"]
     if ptxas_info:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(bdir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -67,15 +75,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs + [
         "-Xlinker", "-rpath," + _cuda_lib_dir()]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="-v" in sys.argv,
+                trace="--trace" in sys.argv))

@@ -10,6 +10,7 @@
 
 #include "cpa.h"
 #include "cpa_attn.cuh"
+#include "cpa_host.h"
 #include "cpa_small.h"
 
 namespace cpa {
@@ -161,17 +162,28 @@ bool plan_geometry(int G, int TS, Geometry& g) {
     return false;
 }
 
+// The dynamic shared-memory limit of a kernel is an attribute of the device's
+// context, so it is raised once per device (and per kernel instance), not once
+// per process: a process that drives several GPUs from one library instance
+// needs it on each of them.
+template <int NUM_MT>
+cudaError_t raise_smem_limit_once() {
+    static PerDevice<int> state;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return (cudaError_t)state.run(dev, (int)cudaErrorInvalidDevice, [](int&) {
+        const int optin = smem_optin();
+        return (int)cudaFuncSetAttribute(paged_attn_kernel<NUM_MT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         optin < kMaxSmemOptin ? optin : kMaxSmemOptin);
+    });
+}
+
 template <int NUM_MT>
 cudaError_t launch_attn(const AttnParams& p, int smem, int grid, cudaStream_t stream) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        const int optin = smem_optin();
-        attr_err = cudaFuncSetAttribute(paged_attn_kernel<NUM_MT>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        optin < kMaxSmemOptin ? optin : kMaxSmemOptin);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    cudaError_t e = raise_smem_limit_once<NUM_MT>();
+    if (e != cudaSuccess) return e;
     if (smem > smem_optin()) return cudaErrorInvalidValue;
     paged_attn_kernel<NUM_MT><<<grid, Cfg<NUM_MT>::kThreads, smem, stream>>>(p);
     return cudaGetLastError();
@@ -725,6 +737,18 @@ cpa_status cpa_debug_wait_timeout(void* workspace, size_t workspace_bytes, int l
                : CPA_ERR_LAUNCH;
 }
 
+#ifdef CPA_TRACE
+// Diagnostic builds only (compiled with -DCPA_TRACE; not part of the product
+// library or its header): point the attention kernel's trace hooks at a
+// caller-owned device buffer laid out as described in cpa_attn.cuh, or at
+// nothing (NULL).  Returns 0 on success.
+int cpa_trace_set_buffer(void* device_buffer) {
+    return cudaMemcpyToSymbol(cpa_trace_buf, &device_buffer, sizeof device_buffer) == cudaSuccess
+               ? 0
+               : 1;
+}
+#endif
+
 int cpa_plan_partition(int64_t total, int n_ctas, int cta, int64_t tile, int64_t* begin,
                        int64_t* end) {
     if (total < 1 || n_ctas < 1 || n_ctas > total || cta < 0 || cta >= n_ctas || tile < 0 ||
@@ -746,20 +770,16 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_scratch[CPA_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+PerDevice<void*> g_scratch_addr;
 
-void* static_scratch_for_current_device() {
+// Device address of this device's copy of the array (looked up on first use).
+cpa_status static_scratch_for_current_device(void** out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = p;
-    }
-    return g_scratch_ptr[dev];
+    if (cudaGetDevice(&dev) != cudaSuccess) return CPA_ERR_CUDA;
+    const int e = g_scratch_addr.run(dev, (int)CPA_ERR_CUDA, [](void*& p) {
+        return cudaGetSymbolAddress(&p, g_static_scratch) == cudaSuccess ? 0 : (int)CPA_ERR_CUDA;
+    }, out);
+    return (cpa_status)e;
 }
 
 }  // namespace
@@ -773,20 +793,33 @@ cpa_status cpa_cascade_verify_noalloc(const void* q, const void* k_pages, const 
                                       int H_kv, int head_dim, int page_size, int num_pages,
                                       int max_prefix_len, float sm_scale, void* o, float* lse,
                                       cpa_stream_t stream) {
-    const size_t need =
-        cpa_cascade_verify_workspace_size(B, topk, S, H_q, H_kv, head_dim, page_size);
+    // the argument checks of the workspace call come first, so a bad size is
+    // reported as such and not as a scratch shortage
+    cpa_status st = check_verify(q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                                 prefix_lens, B, topk, S, H_q, H_kv, head_dim, page_size,
+                                 num_pages, max_prefix_len, sm_scale);
+    if (st != CPA_OK) return st;
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return CPA_ERR_CUDA;
+    // the cascade launch has one work unit per (request, KV head)
+    if (ws_layout((long long)B * H_kv, n_sm).total > (size_t)CPA_STATIC_SCRATCH_BYTES)
+        return CPA_ERR_WORKSPACE;
     void* scratch = nullptr;
-    if (need != 0) {
-        if (need > (size_t)CPA_STATIC_SCRATCH_BYTES) return CPA_ERR_WORKSPACE;
-        scratch = static_scratch_for_current_device();
-        if (!scratch) return CPA_ERR_CUDA;
-    }
-    // need == 0: the sizes are invalid; the shared checks report which error.
+    st = static_scratch_for_current_device(&scratch);
+    if (st != CPA_OK) return st;
     return verify_common(MODE_CASCADE, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
                          draft_page_table, draft_pt_stride, prefix_lens, B, topk, S, H_q, H_kv,
                          head_dim, page_size, num_pages, max_prefix_len, sm_scale, o, lse,
-                         scratch, scratch ? (size_t)CPA_STATIC_SCRATCH_BYTES : 0,
+                         scratch, (size_t)CPA_STATIC_SCRATCH_BYTES,
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+cpa_status cpa_noalloc_device_status(uint32_t* status_out, cpa_stream_t stream) {
+    if (!status_out) return CPA_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    const cpa_status st = static_scratch_for_current_device(&scratch);
+    if (st != CPA_OK) return st;
+    return cpa_get_device_status(scratch, status_out, stream);
 }
 
 }  // extern "C"

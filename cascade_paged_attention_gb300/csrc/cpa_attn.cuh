@@ -54,21 +54,39 @@ constexpr float kRescaleLog2 = 8.0f;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-// Timestamps of pipeline events for a few CTAs, only in builds that define
-// CPA_TRACE (a diagnostic build provides the buffer); otherwise no code.
-// Buffer: [4 CTAs][64 events][1024] clock64 stamps, then every CTA's start and
-// end %globaltimer at kTraceCtaBase + 2 * CTA (+ 0 start, + 1 end).
+// Timestamps of pipeline events, only in builds that define CPA_TRACE (the
+// diagnostic build: `python -m cascade_paged_attention_gb300.build --trace`,
+// whose cpa_trace_set_buffer points cpa_trace_buf at a caller's buffer);
+// otherwise no code.  Buffer layout (64-bit words):
+//   [4 CTAs][64 event rows][1024]  clock64 of event `ev` at tile/unit `idx`
+//                                  for CTAs 0..3 (rows 0..62; row 63 holds
+//                                  those CTAs' start and end clock64 and
+//                                  %globaltimer at indices 0..3);
+//   then kTraceCtaWords words per CTA at kTraceCtaBase + kTraceCtaWords * CTA:
+//     0 start (%globaltimer, after scheduling), 1 end, 2 producer done
+//     issuing, 3 MMA issuer done, 4 epilogue done, 5 tiles, 6 units.
 #ifdef CPA_TRACE
 static __device__ unsigned long long* cpa_trace_buf = nullptr;
 constexpr int kTraceCtaBase = 4 * 64 * 1024;
+constexpr int kTraceCtaWords = 8;
+constexpr int kTraceStampRow = 63;
 #define CPA_TRACE_EVENT(ev, idx)                                                  \
     do {                                                                          \
-        if (cpa_trace_local && blockIdx.x < 4 && (idx) < 1024)                    \
+        if (cpa_trace_local && blockIdx.x < 4 && (ev) < kTraceStampRow &&         \
+            (idx) < 1024)                                                         \
             cpa_trace_local[(blockIdx.x * 64 + (ev)) * 1024 + (idx)] = clock64(); \
+    } while (0)
+#define CPA_TRACE_CTA(slot, value)                                                      \
+    do {                                                                                \
+        if (cpa_trace_local)                                                            \
+            cpa_trace_local[kTraceCtaBase + kTraceCtaWords * blockIdx.x + (slot)] = (value); \
     } while (0)
 #else
 #define CPA_TRACE_EVENT(ev, idx) \
     do {                         \
+    } while (0)
+#define CPA_TRACE_CTA(slot, value) \
+    do {                           \
     } while (0)
 #endif
 
@@ -537,10 +555,11 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
 #ifdef CPA_TRACE
     if (threadIdx.x == 0 && cpa_trace_local) {
         if (blockIdx.x < 4) {
-            cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1000] = clock64();
-            cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1001] = globaltimer_ns();
+            cpa_trace_local[(blockIdx.x * 64 + kTraceStampRow) * 1024 + 0] = clock64();
+            cpa_trace_local[(blockIdx.x * 64 + kTraceStampRow) * 1024 + 1] = globaltimer_ns();
         }
-        cpa_trace_local[kTraceCtaBase + 2 * blockIdx.x] = globaltimer_ns();
+        CPA_TRACE_CTA(0, globaltimer_ns());
+        CPA_TRACE_CTA(5, (unsigned long long)ctrl->count);
     }
 #endif
     const uint32_t tmem = ctrl->tmem_base;
@@ -676,6 +695,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 }
                 w.next(x, jb, je, ctrl);
             }
+            if (lane == 0) CPA_TRACE_CTA(2, globaltimer_ns());
             // make sure no TMA write is still in flight when the CTA leaves
             const long long filled = g;
             for (int st = 0; st < p.n_stages; ++st) {
@@ -822,6 +842,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 }
                 umma_commit(&ctrl->mma_done);
                 mbar_wait(&ctrl->mma_done, 0, abort_flag, p.status);
+                CPA_TRACE_CTA(3, globaltimer_ns());
             }
             __syncwarp();
         } else if (warp >= C::kSmWarp0 && warp < C::kEpiWarp0) {
@@ -1418,6 +1439,10 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 }
                 w.next(x, jb, je, ctrl);
             }
+            if (et == 0) {
+                CPA_TRACE_CTA(4, globaltimer_ns());
+                CPA_TRACE_CTA(6, (unsigned long long)w.seg);
+            }
         }
     }
 
@@ -1426,10 +1451,10 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
 #ifdef CPA_TRACE
     if (threadIdx.x == 0 && cpa_trace_local) {
         if (blockIdx.x < 4) {
-            cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1002] = clock64();
-            cpa_trace_local[(blockIdx.x * 64 + 13) * 1024 + 1003] = globaltimer_ns();
+            cpa_trace_local[(blockIdx.x * 64 + kTraceStampRow) * 1024 + 2] = clock64();
+            cpa_trace_local[(blockIdx.x * 64 + kTraceStampRow) * 1024 + 3] = globaltimer_ns();
         }
-        cpa_trace_local[kTraceCtaBase + 2 * blockIdx.x + 1] = globaltimer_ns();
+        CPA_TRACE_CTA(1, globaltimer_ns());
     }
 #endif
     if (warp == 1) {

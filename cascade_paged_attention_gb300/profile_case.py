@@ -6,6 +6,12 @@
 Generates the seeded workload, runs `warmup` untimed and `iters` timed calls
 on the current stream and prints the mean time per call (CUDA events).  Meant
 to be wrapped by ncu (one kernel name, a few launches).
+
+With ``--trace OUT.json`` it loads the diagnostic build (trace hooks compiled
+in), runs one more call with the trace buffer attached and writes every CTA's
+start, end, producer-done, MMA-done and epilogue-done times (ns from the
+launch's first start) and its tile and unit counts, with a summary of how
+the CTAs' end times spread.
 """
 from __future__ import annotations
 
@@ -34,8 +40,14 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--graph", action="store_true",
                     help="also replay the iters calls from one captured CUDA graph")
+    ap.add_argument("--trace", default="",
+                    help="write per-CTA times of one call (diagnostic build) to this JSON file")
     args = ap.parse_args()
 
+    if args.trace:
+        from cascade_paged_attention_gb300 import build as cbuild
+
+        os.environ["CPA_LIBRARY"] = cbuild.build(trace=True)
     cpa.build_library()
     dev = torch.device("cuda:0")
 
@@ -132,6 +144,48 @@ def main():
         e.record()
         torch.cuda.synchronize()
         print(f"{args.case} {work}: {s.elapsed_time(e) / args.iters * 1e3:.1f} us/call (graph)")
+    if args.trace:
+        trace_one_call(call, args.trace, work)
+
+
+def trace_one_call(call, out_path: str, work: str):
+    """Run `call` once with the trace buffer attached; summarise per-CTA times."""
+    import ctypes
+    import json
+
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    base, per = 4 * 64 * 1024, 8
+    buf = torch.zeros(base + per * n_sm, dtype=torch.int64, device="cuda:0")
+    L = cpa.lib()
+    L.cpa_trace_set_buffer.restype = ctypes.c_int
+    L.cpa_trace_set_buffer.argtypes = [ctypes.c_void_p]
+    if L.cpa_trace_set_buffer(ctypes.c_void_p(buf.data_ptr())) != 0:
+        raise RuntimeError("cpa_trace_set_buffer failed")
+    call()
+    torch.cuda.synchronize()
+    L.cpa_trace_set_buffer(None)
+    cta = buf[base:].view(n_sm, per).cpu().numpy().astype(np.int64)
+    used = cta[:, 5] > 0
+    t0 = int(cta[used, 0].min())
+    rel = lambda col: [int(x - t0) if u else None for x, u in zip(cta[:, col], used)]
+    ends = np.array([int(x - t0) for x, u in zip(cta[:, 1], used) if u])
+    starts = np.array([int(x - t0) for x, u in zip(cta[:, 0], used) if u])
+    summary = {
+        "work": work, "ctas_with_work": int(used.sum()),
+        "start_ns": {"min": int(starts.min()), "max": int(starts.max())},
+        "end_ns": {"min": int(ends.min()), "p10": float(np.percentile(ends, 10)),
+                   "median": float(np.median(ends)), "p90": float(np.percentile(ends, 90)),
+                   "max": int(ends.max())},
+        "tail_ns": int(ends.max() - np.median(ends)),
+        "slowest_ctas": [int(i) for i in np.argsort(-np.where(used, cta[:, 1], 0))[:8]],
+    }
+    out = {"summary": summary,
+           "per_cta": {"start": rel(0), "end": rel(1), "producer_done": rel(2),
+                       "mma_done": rel(3), "epilogue_done": rel(4),
+                       "tiles": [int(x) for x in cta[:, 5]], "units": [int(x) for x in cta[:, 6]]}}
+    with open(out_path, "w") as f:
+        json.dump(out, f)
+    print(json.dumps(summary))
 
 
 if __name__ == "__main__":

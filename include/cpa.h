@@ -39,7 +39,7 @@
  *     DEVICE pointers (16-byte aligned for q, k_pages, v_pages, o) unless a
  *     comment says host.  The caller owns every buffer, including the
  *     workspace; the library never allocates, frees or synchronises (except
- *     cpa_get_device_status, which says so).  Calls are asynchronous on
+ *     cpa_get_device_status and cpa_noalloc_device_status, which say so).  Calls are asynchronous on
  *     `stream` (NULL = legacy default stream) and launch nothing when they
  *     return an error, with one exception: cpa_tree_verify and
  *     cpa_cascade_verify_shared launch more than one kernel, and check every
@@ -53,6 +53,9 @@
  *     workspace-taking call clears that word and the merge counters it uses
  *     (an asynchronous memset on `stream`).  Nothing crosses the ABI as an
  *     exception, and no kernel traps, asserts or prints.
+ *   - When the device status word has any bit set after a call, that call's
+ *     outputs are undefined (they may be partial, stale or computed from a
+ *     truncated mask); only the status word is meaningful.
  *   - A workspace must not be used by two calls that can run at the same time.
  */
 #ifndef CPA_H_
@@ -368,16 +371,26 @@ int cpa_plan_partition(int64_t total, int n_ctas, int cta, int64_t tile, int64_t
  * every device buffer and hands the plugin no allocator.
  *
  * Scratch: a file-scope device array of CPA_STATIC_SCRATCH_BYTES, which every
- * GPU that loads this library holds until the process exits.  Sizes whose
- * workspace (cpa_cascade_verify_workspace_size) exceeds it are rejected with
- * CPA_ERR_WORKSPACE before anything is launched.  The first call on a device,
- * with that device current, looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
- * All calls on a device share the one array and it keeps the last call's
- * contents: each call clears the status word and merge counters it needs
- * (asynchronous memset on `stream`) before its kernel runs.  Calls that
- * overlap on the GPU (different streams, no ordering between them) race on
- * the array.
+ * GPU that loads this library holds until the process exits.  The scratch a
+ * call needs is a fixed part that grows with the device's SM count (two fp32
+ * partial-result slots of 256 rows x 128 columns per SM, about 262 KB per SM,
+ * 40 MB on 152 SMs) plus 4 bytes per (request, KV head).  Sizes that need
+ * more than the array are rejected with CPA_ERR_WORKSPACE before anything
+ * is launched; so the usable shapes shrink as the SM count grows, and on a
+ * part with more than about 180 SMs no shape fits.  Other invalid arguments
+ * get the same status codes as cpa_cascade_verify.
+ *
+ * The first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture.  All calls on a device share the one array and
+ * it keeps the last call's contents: each call clears the status word and
+ * merge counters it needs (asynchronous memset on `stream`) before its
+ * kernel runs.  Calls that overlap on the GPU (different streams, no
+ * ordering between them) race on the array.
+ *
+ * Errors only the GPU can see (bad page id, bad prefix length, wait timeout)
+ * go to the status word at the start of the array; read it with
+ * cpa_noalloc_device_status.
  */
 #define CPA_STATIC_SCRATCH_BYTES (48u * 1024u * 1024u)
 
@@ -388,6 +401,15 @@ cpa_status cpa_cascade_verify_noalloc(const void* q, const void* k_pages, const 
                                       int H_kv, int head_dim, int page_size, int num_pages,
                                       int max_prefix_len, float sm_scale, void* o, float* lse,
                                       cpa_stream_t stream);
+
+/*
+ * The device status word of the static scratch of the current device, as
+ * written by the last cpa_cascade_verify_noalloc call on it, into
+ * *status_out (host).  Same return values as cpa_get_device_status, and
+ * like it SYNCHRONISES `stream`.  The source pages have no counterpart of
+ * this call either.
+ */
+cpa_status cpa_noalloc_device_status(uint32_t* status_out, cpa_stream_t stream);
 
 /* Library version, e.g. 100 for 0.1.0. */
 int cpa_version(void);

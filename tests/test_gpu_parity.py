@@ -80,7 +80,7 @@ def test_merge_state_matches_oracle(cuda_device):
 def test_pass_b_matches_oracle(cuda_device, key):
     wl = _make_small(key)
     d = VerifyDev(wl)
-    o_b, lse_b = cpa.cpa_cascade_pass_b(d.q, d.k, d.v, d.dpt, wl.B, wl.topk, wl.S)
+    o_b, lse_b = cpa.cpa_cascade_pass_b(d.q, d.k, d.v, d.dpt, wl.B, wl.topk, wl.S, check=True)
     torch.cuda.synchronize()
     ref_o, ref_l = oracle.verify_wl(wl, part="draft")
     compare(o_b, lse_b, ref_o, ref_l)
@@ -92,7 +92,7 @@ def test_pass_a_matches_oracle(cuda_device, key):
     wl = _make_small(key)
     d = VerifyDev(wl)
     o_a, lse_a = cpa.cpa_cascade_pass_a(d.q, d.k, d.v, d.ppt, d.lens, wl.topk, wl.S,
-                                        max_prefix_len=wl.max_prefix_len)
+                                        max_prefix_len=wl.max_prefix_len, check=True)
     torch.cuda.synchronize()
     ref_o, ref_l = oracle.verify_wl(wl, part="prefix")
     compare(o_a, lse_a, ref_o, ref_l)
@@ -103,7 +103,7 @@ def test_pass_a_matches_oracle(cuda_device, key):
 def test_cascade_verify_matches_oracle(cuda_device, key):
     wl = _make_small(key)
     d = VerifyDev(wl)
-    o, lse = cpa.cpa_cascade_verify(*d.args(), max_prefix_len=wl.max_prefix_len)
+    o, lse = cpa.cpa_cascade_verify(*d.args(), max_prefix_len=wl.max_prefix_len, check=True)
     torch.cuda.synchronize()
     ref_o, ref_l = oracle.verify_wl(wl)
     compare(o, lse, ref_o, ref_l)
@@ -113,7 +113,8 @@ def test_cascade_verify_matches_oracle(cuda_device, key):
 def test_naive_expand_matches_oracle(cuda_device, key):
     wl = _make_small(key)
     d = VerifyDev(wl)
-    o, lse = cpa.cpa_naive_expand_verify(*d.args(), max_prefix_len=wl.max_prefix_len)
+    o, lse = cpa.cpa_naive_expand_verify(*d.args(), max_prefix_len=wl.max_prefix_len,
+                                         check=True)
     torch.cuda.synchronize()
     ref_o, ref_l = oracle.verify_wl(wl)
     compare(o, lse, ref_o, ref_l)
@@ -177,26 +178,28 @@ def test_full_config_all_rows(cuda_device, name):
     wl = _verify_wl(name)
     d = VerifyDev(wl)
     ref = oracle.verify_wl(wl)
-    o, lse = cpa.cpa_cascade_verify(*d.args(), max_prefix_len=wl.max_prefix_len)
+    o, lse = cpa.cpa_cascade_verify(*d.args(), max_prefix_len=wl.max_prefix_len, check=True)
     torch.cuda.synchronize()
     compare(o, lse, *ref)
-    o, lse = cpa.cpa_naive_expand_verify(*d.args(), max_prefix_len=wl.max_prefix_len)
+    o, lse = cpa.cpa_naive_expand_verify(*d.args(), max_prefix_len=wl.max_prefix_len,
+                                         check=True)
     torch.cuda.synchronize()
     compare(o, lse, *ref)
 
 
-def test_long_variable_config_sampled_rows(cuda_device):
+@pytest.mark.slow
+def test_long_variable_config_all_rows(cuda_device):
+    """Config 4 (per-request L uniform in [1024, 32768], two M tiles): every row."""
     wl = _verify_wl("long_variable")
     d = VerifyDev(wl)
-    n_rows = wl.n_tokens * wl.H_q
-    rows = sample_rows(n_rows, 1536, seed=4, always=[0, n_rows - 1, wl.topk * wl.S * wl.H_q - 1])
-    ref = oracle.verify_wl(wl, rows=rows)
-    o, lse = cpa.cpa_cascade_verify(*d.args(), max_prefix_len=wl.max_prefix_len)
+    ref = oracle.verify_wl(wl)
+    o, lse = cpa.cpa_cascade_verify(*d.args(), max_prefix_len=wl.max_prefix_len, check=True)
     torch.cuda.synchronize()
-    compare(o, lse, *ref, rows=rows)
-    o, lse = cpa.cpa_naive_expand_verify(*d.args(), max_prefix_len=wl.max_prefix_len)
+    compare(o, lse, *ref)
+    o, lse = cpa.cpa_naive_expand_verify(*d.args(), max_prefix_len=wl.max_prefix_len,
+                                         check=True)
     torch.cuda.synchronize()
-    compare(o, lse, *ref, rows=rows)
+    compare(o, lse, *ref)
 
 
 # ------------------------------------------------------------------ prefix-hit prefill
@@ -213,7 +216,7 @@ PREFILL_SMALL = [
 def test_prefill_hit_matches_oracle(cuda_device, cfg, part):
     wl = cpa_synth.make_prefill(**cfg)
     d = PrefillDev(wl)
-    o, lse = cpa.cpa_prefill_hit(d.q, d.k, d.v, d.pt, wl.B, wl.N, wl.H, part=part)
+    o, lse = cpa.cpa_prefill_hit(d.q, d.k, d.v, d.pt, wl.B, wl.N, wl.H, part=part, check=True)
     torch.cuda.synchronize()
     ref = oracle.prefill_wl(wl, part={0: "full", 1: "rect", 2: "tri"}[part])
     compare(o, lse, *ref)
@@ -229,8 +232,42 @@ def test_prefill_rect_tri_merge_equals_full(cuda_device):
     compare(o, lse, *oracle.prefill_wl(wl))
 
 
+def prefill_check_rows(B, M, H, H_q, H_kv, seed, per_request=256):
+    """Rows (token * H_q + head) checked at the full prefill size.
+
+    Every request: `per_request` random suffix tokens with all H_q heads, plus
+    its first and last suffix token.  One (request, KV head) group -- the last
+    request, the last KV head -- additionally gets, for all of its heads, the
+    first and last token of every q tile (so both members of every dealt pair
+    (j, QT-1-j)) and the tokens whose key range ends on a 128-key tile boundary
+    (the diagonal rows of the masked tiles).
+    """
+    G = H_q // H_kv
+    TS = 128 // G
+    rng = np.random.default_rng(seed)
+    toks = set()
+    for b in range(B):
+        pick = rng.choice(M, size=min(per_request, M), replace=False)
+        toks.update(int(b * M + i) for i in pick)
+        toks.update((b * M, b * M + M - 1))
+    rows = set(t * H_q + h for t in toks for h in range(H_q))
+    b, hk = B - 1, H_kv - 1
+    group_toks = set()
+    for p0 in range(0, M, TS):
+        group_toks.update((p0, min(p0 + TS, M) - 1))
+    for i in range(M):
+        if (H + i) % 128 in (0, 127):
+            group_toks.add(i)
+    for i in group_toks:
+        rows.update((b * M + i) * H_q + hk * G + g for g in range(G))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.slow
 @pytest.mark.parametrize("h", [0.0, 0.5, 0.75])
-def test_prefill_full_size_sampled_rows(cuda_device, h):
+def test_prefill_full_size_rows(cuda_device, h):
+    """Config 5 (B=8, N=8192): >= 256 suffix rows per request x all heads, and
+    every q tile's boundary and diagonal rows of one (request, KV head) group."""
     c = cpa_synth.PREFILL_CONFIG
     N = c["N"]
     H = int(h * N)
@@ -238,16 +275,10 @@ def test_prefill_full_size_sampled_rows(cuda_device, h):
                                 page_size=c["page_size"], seed=c["seed"])
     d = PrefillDev(wl)
     M = N - H
-    H_q = wl.H_q
-    # first and last suffix rows of every request plus tile-boundary rows and a random sample
-    special = []
-    for b in range(wl.B):
-        for i in (0, 31, 32, 127, 128, M - 1):
-            if 0 <= i < M:
-                special += [((b * M + i) * H_q + hq) for hq in (0, H_q - 1)]
-    rows = sample_rows(wl.B * M * H_q, 256, seed=int(h * 100), always=special)
+    rows = prefill_check_rows(wl.B, M, H, wl.H_q, wl.H_kv, seed=int(h * 100))
+    assert len(rows) >= wl.B * 256 * wl.H_q
     ref = oracle.prefill_wl(wl, rows=rows)
-    o, lse = cpa.cpa_prefill_hit(d.q, d.k, d.v, d.pt, wl.B, wl.N, wl.H)
+    o, lse = cpa.cpa_prefill_hit(d.q, d.k, d.v, d.pt, wl.B, wl.N, wl.H, check=True)
     torch.cuda.synchronize()
     compare(o, lse, *ref, rows=rows)
 
