@@ -32,6 +32,8 @@ __all__ = [
     "cpa_status_workspace_size",
     "cpa_cascade_verify",
     "cpa_cascade_verify_noalloc",
+    "cpa_cascade_verify_fp8",
+    "cpa_cascade_pass_a_fp8",
     "cpa_naive_expand_verify",
     "cpa_cascade_pass_a",
     "cpa_cascade_pass_b",
@@ -102,6 +104,9 @@ def lib() -> ctypes.CDLL:
         "cpa_cascade_verify": (I, verify_args),
         "cpa_naive_expand_verify": (I, verify_args),
         "cpa_cascade_verify_noalloc": (I, verify_args[:20] + [P]),
+        "cpa_cascade_verify_fp8": (I, verify_args[:3] + [P, P, I] + verify_args[3:]),
+        "cpa_cascade_pass_a_fp8": (I, [P, P, P, P, P, I, P, I, P, I, I, I, I, I, I, I, I, I, F, P,
+                                       P, P, SZ, P]),
         "cpa_cascade_pass_a": (I, [P, P, P, P, I, P, I, I, I, I, I, I, I, I, I, F, P, P, P, SZ,
                                    P]),
         "cpa_cascade_pass_b": (I, [P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
@@ -298,6 +303,95 @@ def cpa_cascade_verify_noalloc(q, k_pages, v_pages, prefix_page_table, draft_pag
         if st != 0:
             raise CpaError(f"cpa_cascade_verify_noalloc (device status word {word:#x})", st)
     return o, lse
+
+
+def _fp8_pools(q, k_pages, v_pages, k_scale, v_scale, prefix_page_table, prefix_lens, topk, S):
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.uint8, 4)
+    _need(v_pages, "v_pages", torch.uint8, 4)
+    _need(k_scale, "k_scale", torch.float32)
+    _need(v_scale, "v_scale", torch.float32)
+    _need(prefix_page_table, "prefix_page_table", torch.int32, 2)
+    _need(prefix_lens, "prefix_lens", torch.int32, 1)
+    if k_pages.shape != v_pages.shape:
+        raise ValueError("k_pages and v_pages must have the same shape")
+    num_pages, P, H_kv, d = k_pages.shape
+    B = prefix_lens.numel()
+    T, H_q, dq = q.shape
+    if dq != d or T != B * topk * S or prefix_page_table.shape[0] != B:
+        raise ValueError("inconsistent verify shapes")
+    n = k_scale.numel()
+    if v_scale.numel() != n or n not in (1, H_kv * d):
+        raise ValueError("k_scale / v_scale must hold 1 or H_kv * head_dim values each")
+    return B, H_q, H_kv, d, P, num_pages, int(n > 1)
+
+
+def cpa_cascade_verify_fp8(q, k_pages, v_pages, k_scale, v_scale, prefix_page_table,
+                           draft_page_table, prefix_lens, topk: int, S: int,
+                           max_prefix_len: Optional[int] = None, sm_scale: Optional[float] = None,
+                           o=None, lse=None, workspace=None, stream=None, check: bool = False):
+    """Cascade verify over FP8 E4M3 KV pages.  Returns (o bf16, lse fp32).
+
+    ``k_pages`` / ``v_pages`` are uint8 E4M3 codes; ``k_scale`` / ``v_scale``
+    fp32 with one value each (per tensor) or ``[H_kv, head_dim]`` (per channel).
+    """
+    B, H_q, H_kv, d, P, num_pages, per_ch = _fp8_pools(q, k_pages, v_pages, k_scale, v_scale,
+                                                       prefix_page_table, prefix_lens, topk, S)
+    _need(draft_page_table, "draft_page_table", torch.int32, 2)
+    if draft_page_table.shape[0] != B * topk:
+        raise ValueError("draft_page_table must have B*topk rows")
+    if max_prefix_len is None:
+        max_prefix_len = prefix_page_table.shape[1] * P
+    if sm_scale is None:
+        sm_scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[0], H_q, dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    ws = _workspace(cpa_cascade_verify_workspace_size(B, topk, S, H_q, H_kv, d, P), q.device,
+                    workspace)
+    st = lib().cpa_cascade_verify_fp8(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale), _ptr(v_scale), per_ch,
+        _ptr(prefix_page_table), prefix_page_table.shape[1], _ptr(draft_page_table),
+        draft_page_table.shape[1], _ptr(prefix_lens), B, topk, S, H_q, H_kv, d, P, num_pages,
+        int(max_prefix_len), float(sm_scale), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+        _stream(stream))
+    _check("cpa_cascade_verify_fp8", st)
+    if check:
+        _check_device("cpa_cascade_verify_fp8", ws, stream)
+    return o, lse
+
+
+def cpa_cascade_pass_a_fp8(q, k_pages, v_pages, k_scale, v_scale, prefix_page_table,
+                           prefix_lens, topk: int, S: int, max_prefix_len: Optional[int] = None,
+                           sm_scale: Optional[float] = None, o_a=None, lse_a=None,
+                           workspace=None, stream=None, check: bool = False):
+    """Pass A alone over FP8 E4M3 KV pages.  Returns (o_a fp32, lse_a fp32)."""
+    B, H_q, H_kv, d, P, num_pages, per_ch = _fp8_pools(q, k_pages, v_pages, k_scale, v_scale,
+                                                       prefix_page_table, prefix_lens, topk, S)
+    if max_prefix_len is None:
+        max_prefix_len = prefix_page_table.shape[1] * P
+    if sm_scale is None:
+        sm_scale = d ** -0.5
+    if o_a is None:
+        o_a = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if lse_a is None:
+        lse_a = torch.empty(q.shape[0], H_q, dtype=torch.float32, device=q.device)
+    _need(o_a, "o_a", torch.float32)
+    _need(lse_a, "lse_a", torch.float32)
+    ws = _workspace(cpa_cascade_verify_workspace_size(B, topk, S, H_q, H_kv, d, P), q.device,
+                    workspace)
+    st = lib().cpa_cascade_pass_a_fp8(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale), _ptr(v_scale), per_ch,
+        _ptr(prefix_page_table), prefix_page_table.shape[1], _ptr(prefix_lens), B, topk, S, H_q,
+        H_kv, d, P, num_pages, int(max_prefix_len), float(sm_scale), _ptr(o_a), _ptr(lse_a),
+        _ptr(ws), ws.numel(), _stream(stream))
+    _check("cpa_cascade_pass_a_fp8", st)
+    if check:
+        _check_device("cpa_cascade_pass_a_fp8", ws, stream)
+    return o_a, lse_a
 
 
 def cpa_naive_expand_verify(q, k_pages, v_pages, prefix_page_table, draft_page_table,

@@ -67,6 +67,22 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t dim1, uint64_t dim2, 
     return r == CUDA_SUCCESS;
 }
 
+// uint8 tensor (FP8 E4M3 codes) [dim2][dim1][128] seen as (d, dim1, dim2),
+// 128-B swizzled boxes of {128, box1, box2}: one box row is a whole 128-code row.
+bool make_map_u8(CUtensorMap* map, const void* base, uint64_t dim1, uint64_t dim2,
+                 uint32_t box1, uint32_t box2) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128, dim1, dim2};
+    cuuint64_t strides[2] = {128, dim1 * 128};
+    cuuint32_t box[3] = {128, box1, box2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 bool page_size_ok(int P) { return P >= 8 && P <= 256 && pow2(P); }
@@ -166,7 +182,7 @@ bool plan_geometry(int G, int TS, Geometry& g) {
 // context, so it is raised once per device (and per kernel instance), not once
 // per process: a process that drives several GPUs from one library instance
 // needs it on each of them.
-template <int NUM_MT>
+template <int NUM_MT, bool FP8>
 cudaError_t raise_smem_limit_once() {
     static PerDevice<int> state;
     int dev = -1;
@@ -174,18 +190,18 @@ cudaError_t raise_smem_limit_once() {
     if (e != cudaSuccess) return e;
     return (cudaError_t)state.run(dev, (int)cudaErrorInvalidDevice, [](int&) {
         const int optin = smem_optin();
-        return (int)cudaFuncSetAttribute(paged_attn_kernel<NUM_MT>,
+        return (int)cudaFuncSetAttribute(paged_attn_kernel<NUM_MT, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          optin < kMaxSmemOptin ? optin : kMaxSmemOptin);
     });
 }
 
-template <int NUM_MT>
+template <int NUM_MT, bool FP8>
 cudaError_t launch_attn(const AttnParams& p, int smem, int grid, cudaStream_t stream) {
-    cudaError_t e = raise_smem_limit_once<NUM_MT>();
+    cudaError_t e = raise_smem_limit_once<NUM_MT, FP8>();
     if (e != cudaSuccess) return e;
     if (smem > smem_optin()) return cudaErrorInvalidValue;
-    paged_attn_kernel<NUM_MT><<<grid, Cfg<NUM_MT>::kThreads, smem, stream>>>(p);
+    paged_attn_kernel<NUM_MT, FP8><<<grid, Cfg<NUM_MT>::kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -215,8 +231,11 @@ cpa_status run_attn(AttnParams& p, const Geometry& geo, long long n_units, void*
     const size_t clear0 = keep_status ? wl.counters : 0;
     if (cudaMemsetAsync(ws + clear0, 0, wl.part_lse - clear0, stream) != cudaSuccess)
         return CPA_ERR_CUDA;
-    cudaError_t e = geo.num_mt == 1 ? launch_attn<1>(p, geo.smem_bytes, n_sm, stream)
-                                    : launch_attn<2>(p, geo.smem_bytes, n_sm, stream);
+    // the FP8 instance exists for one M tile only (Q is staged in TMEM as f16)
+    if (p.fp8 && geo.num_mt != 1) return CPA_ERR_UNSUPPORTED;
+    cudaError_t e = p.fp8 ? launch_attn<1, true>(p, geo.smem_bytes, n_sm, stream)
+                    : geo.num_mt == 1 ? launch_attn<1, false>(p, geo.smem_bytes, n_sm, stream)
+                                      : launch_attn<2, false>(p, geo.smem_bytes, n_sm, stream);
     return e == cudaSuccess ? CPA_OK : CPA_ERR_LAUNCH;
 }
 
@@ -268,25 +287,46 @@ void fill_common(AttnParams& p, const void* q, const void* k_pages, const void* 
     p.scale_log2 = sm_scale * kLog2e;
 }
 
+// K/V pool maps with `rows`-row boxes: bf16 pools in 64-column halves, FP8
+// pools in whole 128-code rows.
+bool pool_map(const AttnParams& p, CUtensorMap* map, const void* base, int H_kv,
+              uint64_t pool_rows, uint32_t rows) {
+    return p.fp8 ? make_map_u8(map, base, H_kv, pool_rows, 1, rows)
+                 : make_map(map, base, H_kv, pool_rows, 1, rows);
+}
+
 bool kv_maps(AttnParams& p, const void* k_pages, const void* v_pages, int H_kv, int num_pages,
              int page_size) {
     const uint64_t rows = (uint64_t)num_pages * page_size;
-    return make_map(&p.kmap, k_pages, H_kv, rows, 1, p.boxr) &&
-           make_map(&p.vmap, v_pages, H_kv, rows, 1, p.boxr);
+    return pool_map(p, &p.kmap, k_pages, H_kv, rows, p.boxr) &&
+           pool_map(p, &p.vmap, v_pages, H_kv, rows, p.boxr);
 }
+
+// Scales of FP8 E4M3 pools: one K and one V value, or [H_kv, 128] each.
+struct Fp8Scales {
+    const float* k_scale;
+    const float* v_scale;
+    int per_channel;
+};
 
 // f32_out: o receives the fp32 result (always for Pass A; for cascade when the
 // result is a partial that a later launch merges).  keep_status: see run_attn.
+// fp8: the pools hold E4M3 codes with these scales (one M tile only).
 cpa_status verify_common(int mode, const void* q, const void* k_pages, const void* v_pages,
                          const int32_t* ppt, int ppt_stride, const int32_t* dpt, int dpt_stride,
                          const int32_t* lens, int B, int topk, int S, int H_q, int H_kv,
                          int head_dim, int page_size, int num_pages, int max_prefix_len,
                          float sm_scale, void* o, float* lse, void* workspace, size_t ws_bytes,
-                         cudaStream_t stream, bool f32_out = false, bool keep_status = false) {
+                         cudaStream_t stream, bool f32_out = false, bool keep_status = false,
+                         const Fp8Scales* fp8 = nullptr) {
     cpa_status st = check_verify(q, k_pages, v_pages, ppt, ppt_stride, lens, B, topk, S, H_q, H_kv,
                                  head_dim, page_size, num_pages, max_prefix_len, sm_scale);
     if (st != CPA_OK) return st;
     if (!o || !lse || !aligned16(o)) return CPA_ERR_INVALID_ARG;
+    if (fp8 && (!fp8->k_scale || !fp8->v_scale ||
+                (reinterpret_cast<uintptr_t>(fp8->k_scale) & 3u) ||
+                (reinterpret_cast<uintptr_t>(fp8->v_scale) & 3u)))
+        return CPA_ERR_INVALID_ARG;
     const bool draft = mode != MODE_PASS_A;
     // The draft tile holds each branch's drafts in a block of sb rows, all read
     // from the branch's first draft page.
@@ -300,9 +340,17 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
     const int TS = mode == MODE_NAIVE ? S : topk * S;
     Geometry geo;
     if (!plan_geometry(G, TS, geo)) return CPA_ERR_UNSUPPORTED;
+    if (fp8 && geo.num_mt != 1) return CPA_ERR_UNSUPPORTED;
     AttnParams p;
     fill_common(p, q, k_pages, v_pages, ppt, ppt_stride, dpt, dpt_stride, lens, B, topk, S, H_q,
                 H_kv, page_size, num_pages, max_prefix_len, sm_scale);
+    if (fp8) {
+        p.fp8 = 1;
+        p.k_scale = fp8->k_scale;
+        p.v_scale = fp8->v_scale;
+        p.scale_per_channel = fp8->per_channel ? 1 : 0;
+        p.scale_log2 *= 256.f;  // the widened K carries 2^-8
+    }
     p.mode = mode;
     p.out_f32 = (mode == MODE_PASS_A || f32_out) ? 1 : 0;
     p.upg = mode == MODE_NAIVE ? topk * H_kv : H_kv;
@@ -318,8 +366,8 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
         const uint64_t rows = (uint64_t)num_pages * page_size;
         // a branch's draft box is exactly its S rows: the rest of the branch block
         // keeps earlier, finite tile data, which P = 0 there multiplies away
-        if (!make_map(&p.kdmap, k_pages, H_kv, rows, 1, S) ||
-            !make_map(&p.vdmap, v_pages, H_kv, rows, 1, S))
+        if (!pool_map(p, &p.kdmap, k_pages, H_kv, rows, S) ||
+            !pool_map(p, &p.vdmap, v_pages, H_kv, rows, S))
             return CPA_ERR_CUDA;
     }
     const long long n_units = (long long)B * p.upg;
@@ -387,6 +435,39 @@ cpa_status cpa_naive_expand_verify(const void* q, const void* k_pages, const voi
                          draft_page_table, draft_pt_stride, prefix_lens, B, topk, S, H_q, H_kv,
                          head_dim, page_size, num_pages, max_prefix_len, sm_scale, o, lse,
                          workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+cpa_status cpa_cascade_verify_fp8(const void* q, const void* k_pages, const void* v_pages,
+                                  const float* k_scale, const float* v_scale,
+                                  int scale_per_channel, const int32_t* prefix_page_table,
+                                  int prefix_pt_stride, const int32_t* draft_page_table,
+                                  int draft_pt_stride, const int32_t* prefix_lens, int B, int topk,
+                                  int S, int H_q, int H_kv, int head_dim, int page_size,
+                                  int num_pages, int max_prefix_len, float sm_scale, void* o,
+                                  float* lse, void* workspace, size_t workspace_bytes,
+                                  cpa_stream_t stream) {
+    const Fp8Scales sc{k_scale, v_scale, scale_per_channel};
+    return verify_common(MODE_CASCADE, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                         draft_page_table, draft_pt_stride, prefix_lens, B, topk, S, H_q, H_kv,
+                         head_dim, page_size, num_pages, max_prefix_len, sm_scale, o, lse,
+                         workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
+                         false, false, &sc);
+}
+
+cpa_status cpa_cascade_pass_a_fp8(const void* q, const void* k_pages, const void* v_pages,
+                                  const float* k_scale, const float* v_scale,
+                                  int scale_per_channel, const int32_t* prefix_page_table,
+                                  int prefix_pt_stride, const int32_t* prefix_lens, int B,
+                                  int topk, int S, int H_q, int H_kv, int head_dim, int page_size,
+                                  int num_pages, int max_prefix_len, float sm_scale, float* o_a,
+                                  float* lse_a, void* workspace, size_t workspace_bytes,
+                                  cpa_stream_t stream) {
+    const Fp8Scales sc{k_scale, v_scale, scale_per_channel};
+    return verify_common(MODE_PASS_A, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                         nullptr, 0, prefix_lens, B, topk, S, H_q, H_kv, head_dim, page_size,
+                         num_pages, max_prefix_len, sm_scale, o_a, lse_a, workspace,
+                         workspace_bytes, reinterpret_cast<cudaStream_t>(stream), false, false,
+                         &sc);
 }
 
 cpa_status cpa_cascade_pass_a(const void* q, const void* k_pages, const void* v_pages,

@@ -122,7 +122,16 @@ struct AttnParams {
     int sb;               // rows per branch block in the draft tile (8 or 16)
     int nbr;              // branches per unit (cascade topk, naive 1)
     int out_f32;          // o is fp32 (a partial for a later merge) instead of bf16
-    float scale_log2;     // sm_scale * log2(e)
+    float scale_log2;     // sm_scale * log2(e) (FP8 pools: times 2^8, see below)
+    // FP8 E4M3 pools (the FP8 kernel instance only): K/V elements are code x
+    // scale, the scale one value per tensor or one per (KV head, channel).
+    // The widened K/V operands carry an extra 2^-8 (e4m3x2_to_f16x2_scaled):
+    // Q is staged as q * k_scale in f16 and scale_log2 includes the 2^8 of K;
+    // the output is multiplied by 2^8 * v_scale per channel at the end.
+    const float* k_scale;
+    const float* v_scale;
+    int scale_per_channel;
+    int fp8;
     uint32_t off_q, off_kv;
 };
 
@@ -234,7 +243,10 @@ __device__ __forceinline__ Unit get_unit(const AttnParams& p, int u) {
         x.n_prefix = x.n_tiles;
         x.trow = p.ptab + (size_t)x.b * p.ptab_stride;
     }
-    x.resid_tile = (x.hi - x.lo) + (p.has_draft ? p.S : 0) <= kResidMaxKeys ? x.n_tiles - 1 : -1;
+    // (f16 P in the FP8 kernel keeps 11 bits: no residual pass there)
+    x.resid_tile = !p.fp8 && (x.hi - x.lo) + (p.has_draft ? p.S : 0) <= kResidMaxKeys
+                       ? x.n_tiles - 1
+                       : -1;
     return x;
 }
 
@@ -247,6 +259,7 @@ struct Ctrl {
     uint64_t o_full, o_empty, stats_full;
     uint64_t mma_done;
     uint64_t merge_full;  // other CTAs' parts of a split unit staged for the merge
+    uint64_t cv_full[4];  // FP8: the stage's codes are widened to f16 operands
     uint32_t tmem_base;
     uint32_t abort_flag;
     int64_t total;   // tiles of the whole problem
@@ -492,7 +505,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-template <int NUM_MT>
+template <int NUM_MT, bool FP8>
 __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     paged_attn_kernel(const __grid_constant__ AttnParams p) {
     using C = Cfg<NUM_MT>;
@@ -514,6 +527,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
         for (int i = 0; i < 4; ++i) {
             mbar_init(&ctrl->kv_full[i], 1);
             mbar_init(&ctrl->kv_empty[i], 1);
+            mbar_init(&ctrl->cv_full[i], 2);  // the two widening warps
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctrl->q_full[i], C::kQInTmem ? 4 : 1);  // 4 epilogue warps / the TMA
@@ -575,6 +589,13 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 is_verify(p.mode) ? l2_policy_evict_first() : l2_policy_evict_normal();
             const uint64_t pol_q = l2_policy_evict_last();
             const int NB = kBN / p.boxr;
+            // TMA copies per box: bf16 K lo/hi and V lo/hi halves (64 columns x
+            // 128 B rows each); FP8 K and V (128 one-byte columns, 128 B rows),
+            // which land in the hi-half regions and are widened in place.
+            // Every copy moves 128 B per row.
+            constexpr int kParts = FP8 ? 2 : 4;
+            auto region = [](int part) { return FP8 ? 2 * part + 1 : part; };
+            auto col0 = [](int part) { return FP8 ? 0 : (part & 1) * 64; };
             const uint32_t q_tx = (uint32_t)(NUM_MT * 2 * G * p.TSB * 128);
             const uint32_t qmt_bytes = (uint32_t)(2 * p.Rq * 128);
             Walker w;
@@ -643,18 +664,18 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         const uint32_t mask = __ballot_sync(0xffffffffu, use);
                         if (lane == 0)
                             mbar_arrive_expect_tx(&ctrl->kv_full[st],
-                                                  (uint32_t)__popc(mask) * 4u * p.S * 128u);
+                                                  (uint32_t)__popc(mask) * kParts * p.S * 128u);
                         __syncwarp();
                         // every lane runs the same iterations (the shuffle needs the whole
                         // warp); only the copy itself is predicated
-                        for (int t0 = 0; t0 < 4 * p.nbr; t0 += 32) {
+                        for (int t0 = 0; t0 < kParts * p.nbr; t0 += 32) {
                             const int t = t0 + lane;
-                            const int k = (t < 4 * p.nbr ? t : 0) >> 2, part = t & 3;
+                            const int k = (t < kParts * p.nbr ? t : 0) / kParts, part = t % kParts;
                             const int pg = __shfl_sync(0xffffffffu, dpage, k & 31);
-                            if (t < 4 * p.nbr && (mask >> k & 1u))
-                                tma_load_3d(stage + part * (kBN * 128) + k * p.sb * 128,
-                                            part < 2 ? &p.kdmap : &p.vdmap, (part & 1) * 64, x.h,
-                                            pg * p.P, &ctrl->kv_full[st], pol_kv);
+                            if (t < kParts * p.nbr && (mask >> k & 1u))
+                                tma_load_3d(stage + region(part) * (kBN * 128) + k * p.sb * 128,
+                                            part < kParts / 2 ? &p.kdmap : &p.vdmap, col0(part),
+                                            x.h, pg * p.P, &ctrl->kv_full[st], pol_kv);
                         }
                         continue;
                     }
@@ -675,20 +696,20 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     const uint32_t mask = __ballot_sync(0xffffffffu, use);
                     if (lane == 0)
                         mbar_arrive_expect_tx(&ctrl->kv_full[st],
-                                              (uint32_t)__popc(mask) * 4u * p.boxr * 128u);
+                                              (uint32_t)__popc(mask) * kParts * p.boxr * 128u);
                     __syncwarp();
                     // One TMA per lane: a thread issues its TMA copies one after another,
-                    // so the 4*NB boxes of a tile are spread over the lanes.  Copy t
-                    // loads part t%4 (K lo/hi, V lo/hi half) of box t/4.  Every lane runs
-                    // the same iterations (the shuffle needs the whole warp).
-                    for (int t0 = 0; t0 < 4 * NB; t0 += 32) {
+                    // so the kParts*NB copies of a tile are spread over the lanes.  Copy
+                    // t loads part t%kParts of box t/kParts.  Every lane runs the same
+                    // iterations (the shuffle needs the whole warp).
+                    for (int t0 = 0; t0 < kParts * NB; t0 += 32) {
                         const int t = t0 + lane;
-                        const int bi = (t < 4 * NB ? t : 0) >> 2, part = t & 3;
+                        const int bi = (t < kParts * NB ? t : 0) / kParts, part = t % kParts;
                         const int pgi = __shfl_sync(0xffffffffu, pg, bi & 31);
-                        if (t < 4 * NB && (mask >> bi & 1u)) {
+                        if (t < kParts * NB && (mask >> bi & 1u)) {
                             const int posi = key_base + (box0 + bi) * p.boxr;
-                            tma_load_3d(stage + part * (kBN * 128) + bi * p.boxr * 128,
-                                        part < 2 ? &p.kmap : &p.vmap, (part & 1) * 64, x.h,
+                            tma_load_3d(stage + region(part) * (kBN * 128) + bi * p.boxr * 128,
+                                        part < kParts / 2 ? &p.kmap : &p.vmap, col0(part), x.h,
                                         pgi * p.P + (posi & (p.P - 1)), &ctrl->kv_full[st], pol_kv);
                         }
                     }
@@ -716,8 +737,14 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             // goes first, so with two M tiles the tensor core works on one M tile
             // while the softmax works on the other.
             if (lane == 0) {
-                const uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
-                const uint32_t idesc_o = idesc_bf16_f32(128, 128, true);
+                // FP8 pools: every operand is f16 (Q, the widened K/V, P)
+                const uint32_t idesc_s =
+                    FP8 ? idesc_f16_f32(128, kBN, false) : idesc_bf16_f32(128, kBN, false);
+                const uint32_t idesc_o =
+                    FP8 ? idesc_f16_f32(128, 128, true) : idesc_bf16_f32(128, 128, true);
+                // the stage is ready for the MMAs when it has landed (bf16) or has
+                // also been widened (FP8); both barriers complete once per use
+                uint64_t* const ready = FP8 ? ctrl->cv_full : ctrl->kv_full;
                 const uint32_t qmt_bytes = (uint32_t)(2 * p.Rq * 128);
                 TileCursor cs, cp;
                 cs.init(ctrl, p);
@@ -741,7 +768,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                             (uint32_t)((p.n_qbufs == 2 ? cs.w.seg >> 1 : cs.w.seg) & 1);
                         const int st = st_s;
                         const bool q_ready = !cs.first() || mbar_test(&ctrl->q_full[qb], qpar);
-                        if (q_ready && mbar_test(&ctrl->kv_full[st], par_s)) {
+                        if (q_ready && mbar_test(&ready[st], par_s)) {
                             if (mt == 0) CPA_TRACE_EVENT(2, gs);
                             tc_fence_after_sync();
                             const int sb = (int)(is & 1);
@@ -824,7 +851,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         if (ip < is)
                             mbar_try_wait_hint(&ctrl->p_full[ip & 1], (uint32_t)((ip >> 1) & 1), 200);
                         else if (is < n_items)
-                            mbar_try_wait_hint(&ctrl->kv_full[st_s], par_s, 200);
+                            mbar_try_wait_hint(&ready[st_s], par_s, 200);
                     }
                     if (!progressed && (++spins & 63u) == 0) {
                         // same time limit as every other wait of the kernel
@@ -845,6 +872,58 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 CPA_TRACE_CTA(3, globaltimer_ns());
             }
             __syncwarp();
+        } else if (FP8 && (warp == 2 || warp == 3)) {
+            // ============================== FP8 widening (warps 2 and 3)
+            // A stage's E4M3 K and V rows land in the hi-half regions (128 codes =
+            // 128 B per row, 128-B swizzled like every operand row).  Each thread
+            // widens whole rows in place: it reads a row's 128 codes, then writes
+            // columns 0..63 as f16 to the lo-half region and columns 64..127 over
+            // the 128 B it read.  Thread ct owns rows ct and ct + 64 of K and of V.
+            // Rows a tile did not load hold earlier finite f16 data (or zeros) and
+            // are widened too, harmlessly: every byte widens to a finite value,
+            // and P = 0 / the mask takes such rows out.
+            const int ct = (int)threadIdx.x - 64;
+            int st = 0;
+            uint32_t par = 0;
+            const long long n_tiles = ctrl->count;
+            for (long long g = 0; g < n_tiles; ++g) {
+                if (!mbar_wait_warp(&ctrl->kv_full[st], par, abort_flag, p.status)) break;
+                uint8_t* stage = smem + p.off_kv + st * kStageBytes;
+#pragma unroll 1
+                for (int i = 0; i < 4; ++i) {
+                    const int kv = i >> 1, r = ct + 64 * (i & 1), sw = r & 7;
+                    uint8_t* lo = stage + (2 * kv) * (kBN * 128) + r * 128;
+                    uint8_t* hi = lo + kBN * 128;
+                    uint4 c[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        c[j] = *reinterpret_cast<const uint4*>(hi + ((j ^ sw) << 4));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        // codes 16j..16j+15 -> f16 columns 16j..16j+15: 16-B chunks
+                        // 2(j%4) and 2(j%4)+1 of the lo (j < 4) or hi half
+                        uint8_t* row = j < 4 ? lo : hi;
+                        const int ca = 2 * (j & 3);
+                        const uint4 a = make_uint4(e4m3x2_to_f16x2_scaled(c[j].x, 0x1404),
+                                                   e4m3x2_to_f16x2_scaled(c[j].x, 0x3424),
+                                                   e4m3x2_to_f16x2_scaled(c[j].y, 0x1404),
+                                                   e4m3x2_to_f16x2_scaled(c[j].y, 0x3424));
+                        const uint4 b = make_uint4(e4m3x2_to_f16x2_scaled(c[j].z, 0x1404),
+                                                   e4m3x2_to_f16x2_scaled(c[j].z, 0x3424),
+                                                   e4m3x2_to_f16x2_scaled(c[j].w, 0x1404),
+                                                   e4m3x2_to_f16x2_scaled(c[j].w, 0x3424));
+                        *reinterpret_cast<uint4*>(row + ((ca ^ sw) << 4)) = a;
+                        *reinterpret_cast<uint4*>(row + (((ca + 1) ^ sw) << 4)) = b;
+                    }
+                }
+                fence_proxy_async_smem();  // the tensor cores read these rows
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctrl->cv_full[st]);
+                if (++st == p.n_stages) {
+                    st = 0;
+                    par ^= 1u;
+                }
+            }
         } else if (warp >= C::kSmWarp0 && warp < C::kEpiWarp0) {
             // ============================== softmax
             // NUM_MT = 1: warpgroup `half` handles columns [64*half, 64*half + 64) of
@@ -1005,10 +1084,10 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                 const float eb =
                                     ex2(fmaf(__uint_as_float(sv[2 * c + 1]), p.scale_log2, -mref));
                                 s4[c & 3] += ea + eb;
-                                pk[c] = pack_bf16x2(ea, eb);
+                                pk[c] = FP8 ? pack_f16x2(ea, eb) : pack_bf16x2(ea, eb);
                             }
                         };
-                        if (!resid) {
+                        if (FP8 || !resid) {
 #pragma unroll 1
                             for (int pc = 0; pc < 2 * kChunks; ++pc) {
                                 const int c0 = half * 64 + (pc >> 1) * 64 * C::kSplit;
@@ -1074,7 +1153,9 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(5, g);
                     if (lane == 0) CPA_TRACE_EVENT(44 + warp - C::kSmWarp0, g);
                     bool zeroed = false;
-                    if (wgi == 0 && !dtile && key0 + kBN > x.valid_end && x.valid_end % p.boxr != 0) {
+                    // (FP8: every byte of a page widens to a finite f16, so nothing to clear)
+                    if (!FP8 && wgi == 0 && !dtile && key0 + kBN > x.valid_end &&
+                        x.valid_end % p.boxr != 0) {
                         // the box holding the sequence's last key was loaded whole: zero
                         // its V rows past the end (whatever the page holds there), so that
                         // P = 0 contributes exactly nothing
@@ -1129,29 +1210,55 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             const int et = r;  // 0..127 within the epilogue warpgroup
             const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
             const bool fp32_out = p.out_f32 != 0;
-            // Q of one unit into TMEM buffer qb: row r is query token r / G, head r % G
+            // Q of one unit into TMEM buffer qb: row r is query token r / G, head r % G.
             auto load_q = [&](const Unit& xu, int qb) {
                 const int it = r / G, gq = r % G;
-                uint32_t v[64];
-                if (it < xu.ntok) {
-                    const uint4* src = reinterpret_cast<const uint4*>(
-                        p.q + ((size_t)(xu.t0 + it) * p.H_q + xu.h * G + gq) * 128);
-                    uint4 u[16];
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    p.q + ((size_t)(xu.t0 + (it < xu.ntok ? it : 0)) * p.H_q + xu.h * G + gq) * 128);
+                if (FP8) {
+                    // FP8 pools: q * k_scale (the unit's KV head) in f16, 32 columns
+                    // (64 channels) at a time
+                    const float* ks = p.k_scale + (p.scale_per_channel ? xu.h * 128 : 0);
+                    const int cs = p.scale_per_channel ? 1 : 0;
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t v[32];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) u[c] = __ldg(src + c);
+                        for (int c = 0; c < 8; ++c) {
+                            uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                            if (it < xu.ntok) u = __ldg(src + hh * 8 + c);
+                            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        v[4 * c] = u[c].x;
-                        v[4 * c + 1] = u[c].y;
-                        v[4 * c + 2] = u[c].z;
-                        v[4 * c + 3] = u[c].w;
+                            for (int k = 0; k < 4; ++k) {
+                                const int ch = (hh * 8 + c) * 8 + 2 * k;  // channel of the low half
+                                v[4 * c + k] = pack_f16x2(__uint_as_float(w[k] << 16) * __ldg(ks + cs * ch),
+                                                          __uint_as_float(w[k] & 0xFFFF0000u) *
+                                                              __ldg(ks + cs * (ch + 1)));
+                            }
+                        }
+                        __syncwarp();
+                        tmem_st_x32(tmem + lane_addr + C::q_col(qb) + 32u * hh, v);
                     }
                 } else {
+                    uint32_t v[64];
+                    if (it < xu.ntok) {
+                        uint4 u[16];
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) v[c] = 0u;
+                        for (int c = 0; c < 16; ++c) u[c] = __ldg(src + c);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            v[4 * c] = u[c].x;
+                            v[4 * c + 1] = u[c].y;
+                            v[4 * c + 2] = u[c].z;
+                            v[4 * c + 3] = u[c].w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) v[c] = 0u;
+                    }
+                    __syncwarp();
+                    tmem_st_x64(tmem + lane_addr + C::q_col(qb), v);
                 }
-                __syncwarp();
-                tmem_st_x64(tmem + lane_addr + C::q_col(qb), v);
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctrl->q_full[qb]);
@@ -1195,6 +1302,15 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         __syncwarp();
                         oa(blk, f);
                         if (!valid) continue;
+                        if (FP8) {
+                            // the widened V carries 2^-8; the V scale is per tensor or
+                            // per (KV head, channel)
+                            const float* vs =
+                                p.v_scale + (p.scale_per_channel ? x.h * 128 + blk * 32 : 0);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                f[e] *= 256.f * __ldg(vs + (p.scale_per_channel ? e : 0));
+                        }
                         if (fp32_out) {
                             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) +
                                                                     orow * 128 + blk * 32);

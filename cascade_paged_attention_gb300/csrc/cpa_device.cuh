@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "cpa_types.h"
 
@@ -249,6 +250,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f16 with f16 A and B (both the same type, as
+// the instruction requires), D fp32: the A/B format fields are 0.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
+    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
 //   bits 0-13 start >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte offset >> 4,
 //   46-47 = 1 (tcgen05 descriptor), 49-51 base offset (0: start within the
@@ -398,6 +406,29 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// FP8 E4M3 -> f16, scaled by 2^-8, for two codes at a time.  An E4M3 code
+// s.eeee.mmm (exponent bias 7, subnormals at exponent 0) placed with its
+// seven magnitude bits at f16 bits 7..13 and its sign at bit 15 is, read as
+// an f16 (bias 15), exactly its value times 2^-8: normals land on exponent
+// field eeee (so 2^(e-15) = 2^(e-7) * 2^-8) and subnormals on f16
+// subnormals with the same mantissa bits.  Every code maps to a finite f16
+// (the two NaN codes read as +-480 * 2^-8), so stale or garbage bytes can
+// never inject a NaN into the tensor-core operands.
+//   w    four codes (byte 0 = first element)
+//   sel  0x1404: codes 0, 1 -> result; 0x3424: codes 2, 3 -> result
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w, uint32_t sel) {
+    uint32_t t;
+    // each code to the high byte of a 16-bit lane: sign at bit 15, magnitude at 8..14
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(w), "r"(sel));
+    const uint32_t u = t >> 1;  // magnitude to bits 7..13, sign to bit 14 (bit 15 is 0)
+    return u + (u & 0x40004000u);  // carry the sign from bit 14 up to bit 15
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {

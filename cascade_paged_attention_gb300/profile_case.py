@@ -31,10 +31,11 @@ import cpa_synth  # noqa: E402
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", choices=["cascade", "naive", "pass_a", "pass_b", "prefill", "tree",
-                                       "tree_pass_b", "shared"],
+                                       "tree_pass_b", "shared", "cascade_fp8"],
                     default="cascade")
     ap.add_argument("--config", default="pages_example")
     ap.add_argument("--hit", type=float, default=0.5, help="prefill: cached fraction h")
+    ap.add_argument("--scales", default="channel", help="cascade_fp8: tensor or channel")
     ap.add_argument("--batch", type=int, default=0, help="override B")
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--iters", type=int, default=3)
@@ -69,6 +70,23 @@ def main():
         def call():
             cpa.cpa_prefill_hit(q, kp, vp, pt, wl.B, wl.N, wl.H)
         work = f"prefill B={wl.B} N={wl.N} H={wl.H}: {wl.visible_pairs() * wl.B * wl.H_q} pairs"
+    elif args.case == "cascade_fp8":
+        cfg = dict(cpa_synth.VERIFY_CONFIGS[args.config])
+        if args.batch:
+            cfg["B"] = args.batch
+        wl = cpa_synth.make_verify_fp8(scales=args.scales, **cfg)
+        q = bf(wl.q)
+        kp = torch.from_numpy(np.ascontiguousarray(wl.k_pages)).to(dev)
+        vp = torch.from_numpy(np.ascontiguousarray(wl.v_pages)).to(dev)
+        ks = torch.from_numpy(np.ascontiguousarray(wl.k_scale, dtype=np.float32)).to(dev)
+        vs = torch.from_numpy(np.ascontiguousarray(wl.v_scale, dtype=np.float32)).to(dev)
+        ppt, dpt, lens = i32(wl.prefix_page_table), i32(wl.draft_page_table), i32(wl.prefix_lens)
+        mpl = wl.max_prefix_len
+
+        def call():
+            cpa.cpa_cascade_verify_fp8(q, kp, vp, ks, vs, ppt, dpt, lens, wl.topk, wl.S, mpl)
+        work = (f"{args.config} FP8 ({args.scales} scales): unique KV "
+                f"{wl.unique_kv_tokens() * wl.kv_bytes_per_token() / 1e6:.1f} MB")
     elif args.case == "shared":
         cfg = dict(cpa_synth.SHARED_CONFIGS[args.config])
         wl = cpa_synth.make_shared_verify(**cfg)

@@ -468,12 +468,14 @@ class Fp8VerifyWorkload:
 def make_verify_fp8(B: int, topk: int, S: int, H_q: int, H_kv: int, head_dim: int = 128,
                     page_size: int = 16, L: Optional[int] = None, prefix_lens=None,
                     scales: str = "tensor", seed: int = 0,
-                    perm_seed: Optional[int] = None) -> Fp8VerifyWorkload:
+                    perm_seed: Optional[int] = None,
+                    pad_code: Optional[int] = None) -> Fp8VerifyWorkload:
     """Build a verify workload over FP8 pools.
 
     ``scales``: ``"tensor"`` (one random K and one random V scale), ``"channel"``
     (one per KV head and channel), ``"unit"`` (both 1.0) or ``"pow2"`` (per
-    channel, random powers of two).  Unused page slots hold random codes.
+    channel, random powers of two).  Unused page slots hold random codes, or
+    the byte ``pad_code`` when it is given (e.g. 0x7F, a NaN code).
     """
     rng = np.random.default_rng(seed)
     if prefix_lens is not None:
@@ -492,6 +494,11 @@ def make_verify_fp8(B: int, topk: int, S: int, H_q: int, H_kv: int, head_dim: in
     for n in counts:
         tables.append(perm[cur:cur + n].copy())
         cur += n
+    if pad_code is not None:
+        for tab, n in zip(tables, seqs):
+            pos = np.arange(n, len(tab) * P)
+            k_pages[tab[pos // P], pos % P] = np.uint8(pad_code)
+            v_pages[tab[pos // P], pos % P] = np.uint8(pad_code)
     if scales == "tensor":
         k_scale = rng.uniform(0.25, 2.0, size=1).astype(np.float32)
         v_scale = rng.uniform(0.25, 2.0, size=1).astype(np.float32)

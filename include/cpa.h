@@ -201,6 +201,49 @@ cpa_status cpa_merge_state(const float* o_a, const float* lse_a, const float* o_
                            float* lse_out, cpa_stream_t stream);
 
 /*
+ * Cascade verify over FP8 KV pages (KV-cache tutorial, section 4.5 "FP8 KV":
+ * half the bytes of bf16, with a per-tensor or per-channel scale).  Same
+ * arguments, layout, token order and results as cpa_cascade_verify, except:
+ *   k_pages, v_pages   uint8 [num_pages, page_size, H_kv, head_dim] E4M3 codes
+ *                      (1 sign, 4 exponent bits with bias 7, 3 mantissa bits;
+ *                      exponent 0 holds zero and subnormals); element value =
+ *                      decoded code x scale.
+ *   k_scale, v_scale   fp32 on the device: one value each when
+ *                      scale_per_channel is 0, else [H_kv, head_dim] each
+ *                      (one scale per KV head and channel).
+ * q stays bf16 and o bf16, lse fp32.  The two NaN codes (0x7F, 0xFF) must not
+ * appear in slots a row sees: they are read as +-480 x scale, not as NaN
+ * (every other code is exact).  Slots past a sequence's end may hold any byte.
+ * Arithmetic: codes are widened exactly to f16 on chip; q x k_scale is
+ * rounded to f16 once (so |q x k_scale| must stay below 65504), P is f16,
+ * accumulation fp32.  Supported: as for cpa_cascade_verify, and
+ * topk*S*(H_q/H_kv) <= 128 (one M tile).  Workspace:
+ * cpa_cascade_verify_workspace_size.
+ */
+cpa_status cpa_cascade_verify_fp8(const void* q, const void* k_pages, const void* v_pages,
+                                  const float* k_scale, const float* v_scale,
+                                  int scale_per_channel, const int32_t* prefix_page_table,
+                                  int prefix_pt_stride, const int32_t* draft_page_table,
+                                  int draft_pt_stride, const int32_t* prefix_lens, int B, int topk,
+                                  int S, int H_q, int H_kv, int head_dim, int page_size,
+                                  int num_pages, int max_prefix_len, float sm_scale, void* o,
+                                  float* lse, void* workspace, size_t workspace_bytes,
+                                  cpa_stream_t stream);
+
+/*
+ * Pass A alone over FP8 KV pages: cpa_cascade_pass_a's result (fp32 o_a,
+ * lse_a) with the pools and scales of cpa_cascade_verify_fp8.
+ */
+cpa_status cpa_cascade_pass_a_fp8(const void* q, const void* k_pages, const void* v_pages,
+                                  const float* k_scale, const float* v_scale,
+                                  int scale_per_channel, const int32_t* prefix_page_table,
+                                  int prefix_pt_stride, const int32_t* prefix_lens, int B,
+                                  int topk, int S, int H_q, int H_kv, int head_dim, int page_size,
+                                  int num_pages, int max_prefix_len, float sm_scale, float* o_a,
+                                  float* lse_a, void* workspace, size_t workspace_bytes,
+                                  cpa_stream_t stream);
+
+/*
  * Bytes of workspace cpa_prefill_hit needs for these sizes on the current
  * device (0 for sizes it would reject).
  */
