@@ -349,7 +349,6 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
         p.k_scale = fp8->k_scale;
         p.v_scale = fp8->v_scale;
         p.scale_per_channel = fp8->per_channel ? 1 : 0;
-        p.scale_log2 *= 256.f;  // the widened K carries 2^-8
     }
     p.mode = mode;
     p.out_f32 = (mode == MODE_PASS_A || f32_out) ? 1 : 0;

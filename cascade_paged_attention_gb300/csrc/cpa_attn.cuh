@@ -122,12 +122,13 @@ struct AttnParams {
     int sb;               // rows per branch block in the draft tile (8 or 16)
     int nbr;              // branches per unit (cascade topk, naive 1)
     int out_f32;          // o is fp32 (a partial for a later merge) instead of bf16
-    float scale_log2;     // sm_scale * log2(e) (FP8 pools: times 2^8, see below)
+    float scale_log2;     // sm_scale * log2(e)
     // FP8 E4M3 pools (the FP8 kernel instance only): K/V elements are code x
     // scale, the scale one value per tensor or one per (KV head, channel).
-    // The widened K/V operands carry an extra 2^-8 (e4m3x2_to_f16x2_scaled):
-    // Q is staged as q * k_scale in f16 and scale_log2 includes the 2^8 of K;
-    // the output is multiplied by 2^8 * v_scale per channel at the end.
+    // K codes are widened exactly (e4m3x2_to_f16x2) and Q is staged as
+    // q * k_scale in f16; V codes are widened with an extra 2^-8
+    // (e4m3x2_to_f16x2_scaled, which never yields a NaN), so the output is
+    // multiplied by 2^8 * v_scale per channel at the end.
     const float* k_scale;
     const float* v_scale;
     int scale_per_channel;
@@ -525,7 +526,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 4; ++i) {
-            mbar_init(&ctrl->kv_full[i], 1);
+            mbar_init(&ctrl->kv_full[i], FP8 ? 1 : 2);  // one arrival per producer warp
             mbar_init(&ctrl->kv_empty[i], 1);
             mbar_init(&ctrl->cv_full[i], 2);  // the two widening warps
         }
@@ -582,8 +583,10 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     const int G = p.G;
 
     if (ctrl->count > 0) {
-        if (warp == 0) {
-            // ============================== producer
+        if (warp == 0 || (!FP8 && warp == 2)) {
+            // ============================== producers
+            // bf16: warp 0 loads the K halves of every box and warp 2 the V halves
+            // (two warps issue TMA copies faster than one); FP8: warp 0 loads both.
             // verify reads each K/V tile once; prefill reads it once per q tile
             const uint64_t pol_kv =
                 is_verify(p.mode) ? l2_policy_evict_first() : l2_policy_evict_normal();
@@ -596,6 +599,9 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             constexpr int kParts = FP8 ? 2 : 4;
             auto region = [](int part) { return FP8 ? 2 * part + 1 : part; };
             auto col0 = [](int part) { return FP8 ? 0 : (part & 1) * 64; };
+            // this warp's copies: parts [kPP * pi, kPP * pi + kPP) of every box
+            constexpr int kPP = FP8 ? kParts : kParts / 2;
+            const int pi = warp == 0 ? 0 : 1;
             const uint32_t q_tx = (uint32_t)(NUM_MT * 2 * G * p.TSB * 128);
             const uint32_t qmt_bytes = (uint32_t)(2 * p.Rq * 128);
             Walker w;
@@ -608,7 +614,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 const Unit x = get_unit(p, w.u);
                 int jb, je;
                 w.piece(x, jb, je);
-                if (!C::kQInTmem) {
+                if (!C::kQInTmem && pi == 0) {
                     const int qb = w.seg % p.n_qbufs;
                     if (w.seg >= p.n_qbufs)
                         ok = mbar_wait_warp(&ctrl->q_empty[qb], ((w.seg / p.n_qbufs) - 1) & 1,
@@ -664,15 +670,16 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         const uint32_t mask = __ballot_sync(0xffffffffu, use);
                         if (lane == 0)
                             mbar_arrive_expect_tx(&ctrl->kv_full[st],
-                                                  (uint32_t)__popc(mask) * kParts * p.S * 128u);
+                                                  (uint32_t)__popc(mask) * kPP * p.S * 128u);
                         __syncwarp();
                         // every lane runs the same iterations (the shuffle needs the whole
                         // warp); only the copy itself is predicated
-                        for (int t0 = 0; t0 < kParts * p.nbr; t0 += 32) {
+                        for (int t0 = 0; t0 < kPP * p.nbr; t0 += 32) {
                             const int t = t0 + lane;
-                            const int k = (t < kParts * p.nbr ? t : 0) / kParts, part = t % kParts;
+                            const int k = (t < kPP * p.nbr ? t : 0) / kPP;
+                            const int part = kPP * pi + t % kPP;
                             const int pg = __shfl_sync(0xffffffffu, dpage, k & 31);
-                            if (t < kParts * p.nbr && (mask >> k & 1u))
+                            if (t < kPP * p.nbr && (mask >> k & 1u))
                                 tma_load_3d(stage + region(part) * (kBN * 128) + k * p.sb * 128,
                                             part < kParts / 2 ? &p.kdmap : &p.vdmap, col0(part),
                                             x.h, pg * p.P, &ctrl->kv_full[st], pol_kv);
@@ -696,17 +703,18 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     const uint32_t mask = __ballot_sync(0xffffffffu, use);
                     if (lane == 0)
                         mbar_arrive_expect_tx(&ctrl->kv_full[st],
-                                              (uint32_t)__popc(mask) * kParts * p.boxr * 128u);
+                                              (uint32_t)__popc(mask) * kPP * p.boxr * 128u);
                     __syncwarp();
                     // One TMA per lane: a thread issues its TMA copies one after another,
-                    // so the kParts*NB copies of a tile are spread over the lanes.  Copy
-                    // t loads part t%kParts of box t/kParts.  Every lane runs the same
+                    // so the kPP*NB copies of this warp are spread over the lanes.  Copy
+                    // t loads part kPP*pi + t%kPP of box t/kPP.  Every lane runs the same
                     // iterations (the shuffle needs the whole warp).
-                    for (int t0 = 0; t0 < kParts * NB; t0 += 32) {
+                    for (int t0 = 0; t0 < kPP * NB; t0 += 32) {
                         const int t = t0 + lane;
-                        const int bi = (t < kParts * NB ? t : 0) / kParts, part = t % kParts;
+                        const int bi = (t < kPP * NB ? t : 0) / kPP;
+                        const int part = kPP * pi + t % kPP;
                         const int pgi = __shfl_sync(0xffffffffu, pg, bi & 31);
-                        if (t < kParts * NB && (mask >> bi & 1u)) {
+                        if (t < kPP * NB && (mask >> bi & 1u)) {
                             const int posi = key_base + (box0 + bi) * p.boxr;
                             tma_load_3d(stage + region(part) * (kBN * 128) + bi * p.boxr * 128,
                                         part < kParts / 2 ? &p.kmap : &p.vmap, col0(part), x.h,
@@ -873,26 +881,27 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             }
             __syncwarp();
         } else if (FP8 && (warp == 2 || warp == 3)) {
-            // ============================== FP8 widening (warps 2 and 3)
-            // A stage's E4M3 K and V rows land in the hi-half regions (128 codes =
-            // 128 B per row, 128-B swizzled like every operand row).  Each thread
-            // widens whole rows in place: it reads a row's 128 codes, then writes
-            // columns 0..63 as f16 to the lo-half region and columns 64..127 over
-            // the 128 B it read.  Thread ct owns rows ct and ct + 64 of K and of V.
-            // Rows a tile did not load hold earlier finite f16 data (or zeros) and
-            // are widened too, harmlessly: every byte widens to a finite value,
-            // and P = 0 / the mask takes such rows out.
+            // ============================== FP8: widening K (warps 2 and 3)
+            // A stage's E4M3 K rows land in the K hi-half region (128 codes = 128 B
+            // per row, 128-B swizzled like every operand row).  Each thread widens
+            // whole rows in place: it reads a row's 128 codes, then writes columns
+            // 0..63 as f16 to the lo-half region and columns 64..127 over the 128 B
+            // it read.  Thread ct owns rows ct and ct + 64; the S MMA waits for
+            // both warps (cv_full).  (V is widened by the softmax warps, before
+            // they need the tile's P: PV waits for them anyway.)  Rows a tile did
+            // not load hold stale data, widened too; their columns are masked.
             const int ct = (int)threadIdx.x - 64;
             int st = 0;
             uint32_t par = 0;
             const long long n_tiles = ctrl->count;
             for (long long g = 0; g < n_tiles; ++g) {
                 if (!mbar_wait_warp(&ctrl->kv_full[st], par, abort_flag, p.status)) break;
+                if (ct == 0) CPA_TRACE_EVENT(57, g);
                 uint8_t* stage = smem + p.off_kv + st * kStageBytes;
 #pragma unroll 1
-                for (int i = 0; i < 4; ++i) {
-                    const int kv = i >> 1, r = ct + 64 * (i & 1), sw = r & 7;
-                    uint8_t* lo = stage + (2 * kv) * (kBN * 128) + r * 128;
+                for (int i = 0; i < 2; ++i) {
+                    const int r = ct + 64 * i, sw = r & 7;
+                    uint8_t* lo = stage + r * 128;
                     uint8_t* hi = lo + kBN * 128;
                     uint4 c[8];
 #pragma unroll
@@ -904,14 +913,14 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         // 2(j%4) and 2(j%4)+1 of the lo (j < 4) or hi half
                         uint8_t* row = j < 4 ? lo : hi;
                         const int ca = 2 * (j & 3);
-                        const uint4 a = make_uint4(e4m3x2_to_f16x2_scaled(c[j].x, 0x1404),
-                                                   e4m3x2_to_f16x2_scaled(c[j].x, 0x3424),
-                                                   e4m3x2_to_f16x2_scaled(c[j].y, 0x1404),
-                                                   e4m3x2_to_f16x2_scaled(c[j].y, 0x3424));
-                        const uint4 b = make_uint4(e4m3x2_to_f16x2_scaled(c[j].z, 0x1404),
-                                                   e4m3x2_to_f16x2_scaled(c[j].z, 0x3424),
-                                                   e4m3x2_to_f16x2_scaled(c[j].w, 0x1404),
-                                                   e4m3x2_to_f16x2_scaled(c[j].w, 0x3424));
+                        const uint4 a = make_uint4(e4m3x2_to_f16x2(c[j].x, false),
+                                                   e4m3x2_to_f16x2(c[j].x, true),
+                                                   e4m3x2_to_f16x2(c[j].y, false),
+                                                   e4m3x2_to_f16x2(c[j].y, true));
+                        const uint4 b = make_uint4(e4m3x2_to_f16x2(c[j].z, false),
+                                                   e4m3x2_to_f16x2(c[j].z, true),
+                                                   e4m3x2_to_f16x2(c[j].w, false),
+                                                   e4m3x2_to_f16x2(c[j].w, true));
                         *reinterpret_cast<uint4*>(row + ((ca ^ sw) << 4)) = a;
                         *reinterpret_cast<uint4*>(row + (((ca + 1) ^ sw) << 4)) = b;
                     }
@@ -919,6 +928,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 fence_proxy_async_smem();  // the tensor cores read these rows
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctrl->cv_full[st]);
+                if (ct == 0) CPA_TRACE_EVENT(58, g);
                 if (++st == p.n_stages) {
                     st = 0;
                     par ^= 1u;
@@ -942,6 +952,8 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             Walker w;
             w.init(ctrl);
             long long g = 0;
+            int vst = 0;         // FP8: stage of tile g and the parity of its use
+            uint32_t vpar = 0;
             bool ok = true;
             while (w.left > 0 && ok) {
                 const Unit x = get_unit(p, w.u);
@@ -962,7 +974,48 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     const int sb = (int)(g % C::kSBufs);
                     const int bi = C::kSBufs == 2 ? sb : mt;
                     const uint32_t par = (uint32_t)((C::kSBufs == 2 ? g >> 1 : g) & 1);
-                    bool okl = mbar_wait_warp(&ctrl->s_full[bi], par, abort_flag, p.status);
+                    bool okv = true;
+                    if (FP8) {
+                        // widen this tile's V codes (the PV MMA waits for these warps'
+                        // P anyway): thread 2r + hh widens columns 64hh..64hh+63 of V
+                        // row r, in place like the K rows.  The row's two threads are in
+                        // one warp: both read the row's codes before either writes.
+                        okv = mbar_wait_warp(&ctrl->kv_full[vst], vpar, abort_flag, p.status);
+                        if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(59, g);
+                        if (okv) {
+                            const int sidx = (int)threadIdx.x - C::kSmWarp0 * 32;
+                            const int vr = sidx >> 1, hh = sidx & 1, sw = vr & 7;
+                            uint8_t* vlo = smem + p.off_kv + vst * kStageBytes + 2 * kBN * 128 +
+                                           vr * 128;
+                            uint8_t* vhi = vlo + kBN * 128;
+                            uint4 c[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                c[j] = *reinterpret_cast<const uint4*>(vhi + (((4 * hh + j) ^ sw) << 4));
+                            __syncwarp();
+                            uint8_t* row = hh ? vhi : vlo;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint4 a = make_uint4(e4m3x2_to_f16x2_scaled(c[j].x, 0x1404),
+                                                           e4m3x2_to_f16x2_scaled(c[j].x, 0x3424),
+                                                           e4m3x2_to_f16x2_scaled(c[j].y, 0x1404),
+                                                           e4m3x2_to_f16x2_scaled(c[j].y, 0x3424));
+                                const uint4 b = make_uint4(e4m3x2_to_f16x2_scaled(c[j].z, 0x1404),
+                                                           e4m3x2_to_f16x2_scaled(c[j].z, 0x3424),
+                                                           e4m3x2_to_f16x2_scaled(c[j].w, 0x1404),
+                                                           e4m3x2_to_f16x2_scaled(c[j].w, 0x3424));
+                                *reinterpret_cast<uint4*>(row + (((2 * j) ^ sw) << 4)) = a;
+                                *reinterpret_cast<uint4*>(row + (((2 * j + 1) ^ sw) << 4)) = b;
+                            }
+                            fence_proxy_async_smem();  // PV reads these rows
+                        }
+                        if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(60, g);
+                        if (++vst == p.n_stages) {
+                            vst = 0;
+                            vpar ^= 1u;
+                        }
+                    }
+                    bool okl = okv && mbar_wait_warp(&ctrl->s_full[bi], par, abort_flag, p.status);
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(4, g);
                     if (lane == 0) CPA_TRACE_EVENT(20 + warp - C::kSmWarp0, g);
                     const bool dtile = jj >= x.n_prefix;

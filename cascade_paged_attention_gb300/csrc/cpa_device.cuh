@@ -431,6 +431,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w, uint32_t 
     return u + (u & 0x40004000u);  // carry the sign from bit 14 up to bit 15
 }
 
+// FP8 E4M3 -> f16, exact, two codes at a time (the PTX conversion; the NaN
+// codes stay NaN).  `w`: four codes, byte 0 first; `hi` picks codes 2, 3.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w, bool hi) {
+    uint32_t r;
+    const uint16_t h = (uint16_t)(hi ? (w >> 16) : (w & 0xFFFFu));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+    return r;
+}
+
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll

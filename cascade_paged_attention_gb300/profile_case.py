@@ -183,6 +183,9 @@ def trace_one_call(call, out_path: str, work: str):
     torch.cuda.synchronize()
     L.cpa_trace_set_buffer(None)
     cta = buf[base:].view(n_sm, per).cpu().numpy().astype(np.int64)
+    # the per-tile event rows of CTAs 0..3 (clock64 stamps), for a closer look
+    np.save(os.path.splitext(out_path)[0] + "_events.npy",
+            buf[:base].view(4, 64, 1024).cpu().numpy())
     used = cta[:, 5] > 0
     t0 = int(cta[used, 0].min())
     rel = lambda col: [int(x - t0) if u else None for x, u in zip(cta[:, col], used)]

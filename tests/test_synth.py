@@ -113,3 +113,28 @@ def test_fp8_codes_have_no_nan_and_order_one_magnitudes():
     expo = (c >> 3) & 0xF
     assert set(np.unique(expo).tolist()) <= {0, 5, 6, 7, 8}
     assert (expo == 0).mean() < 0.05
+
+
+def test_fp8_logical_contents_do_not_depend_on_placement():
+    """The FP8 generator keeps the logical K/V of every sequence fixed by `seed`
+    whatever the page permutation (`perm_seed`), like the bf16 generator."""
+    kw = dict(B=3, topk=2, S=3, H_q=8, H_kv=2, page_size=8, prefix_lens=[20, 0, 9], seed=5)
+    a = cpa_synth.make_verify_fp8(perm_seed=1, **kw)
+    b = cpa_synth.make_verify_fp8(perm_seed=2, **kw)
+    assert not np.array_equal(a.prefix_page_table, b.prefix_page_table)
+
+    def logical(wl, tab, n):
+        pos = np.arange(n)
+        return wl.k_pages[tab[pos // wl.page_size], pos % wl.page_size], \
+            wl.v_pages[tab[pos // wl.page_size], pos % wl.page_size]
+
+    for r in range(kw["B"]):
+        n = int(a.prefix_lens[r])
+        for x, y in zip(logical(a, a.prefix_page_table[r], n), logical(b, b.prefix_page_table[r], n)):
+            assert np.array_equal(x, y)
+    for v in range(kw["B"] * kw["topk"]):
+        for x, y in zip(logical(a, a.draft_page_table[v], kw["S"]),
+                        logical(b, b.draft_page_table[v], kw["S"])):
+            assert np.array_equal(x, y)
+    assert np.array_equal(a.q, b.q)
+    assert np.array_equal(a.k_scale, b.k_scale)
