@@ -125,10 +125,8 @@ struct AttnParams {
     float scale_log2;     // sm_scale * log2(e)
     // FP8 E4M3 pools (the FP8 kernel instance only): K/V elements are code x
     // scale, the scale one value per tensor or one per (KV head, channel).
-    // K codes are widened exactly (e4m3x2_to_f16x2) and Q is staged as
-    // q * k_scale in f16; V codes are widened with an extra 2^-8
-    // (e4m3x2_to_f16x2_scaled, which never yields a NaN), so the output is
-    // multiplied by 2^8 * v_scale per channel at the end.
+    // Codes are widened exactly to f16 (e4m3x2_to_f16x2); Q is staged as
+    // q * k_scale in f16 and the output multiplied by v_scale per channel.
     const float* k_scale;
     const float* v_scale;
     int scale_per_channel;
@@ -260,7 +258,11 @@ struct Ctrl {
     uint64_t o_full, o_empty, stats_full;
     uint64_t mma_done;
     uint64_t merge_full;  // other CTAs' parts of a split unit staged for the merge
-    uint64_t cv_full[4];  // FP8: the stage's codes are widened to f16 operands
+    uint64_t cv_full[4];   // FP8: the stage's K codes are widened to f16
+    uint64_t cvv_full[4];  // FP8: the stage's V codes are widened to f16
+    // FP8: bit r of vrows[stage][r / 32]: V row r of the stage's tile holds a key
+    // of the sequence (loaded, before the end); other V rows are zeroed
+    uint32_t vrows[4][4];
     uint32_t tmem_base;
     uint32_t abort_flag;
     int64_t total;   // tiles of the whole problem
@@ -529,6 +531,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             mbar_init(&ctrl->kv_full[i], FP8 ? 1 : 2);  // one arrival per producer warp
             mbar_init(&ctrl->kv_empty[i], 1);
             mbar_init(&ctrl->cv_full[i], 2);  // the two widening warps
+            mbar_init(&ctrl->cvv_full[i], 2);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctrl->q_full[i], C::kQInTmem ? 4 : 1);  // 4 epilogue warps / the TMA
@@ -668,6 +671,17 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                             use = false;
                         }
                         const uint32_t mask = __ballot_sync(0xffffffffu, use);
+                        if (FP8 && lane == 0) {
+                            // rows k*sb .. k*sb+S-1 of every loaded branch k
+                            uint32_t vr[4] = {0u, 0u, 0u, 0u};
+                            for (int k = 0; k < p.nbr; ++k)
+                                if (mask >> k & 1u)
+                                    for (int s2 = 0; s2 < p.S; ++s2) {
+                                        const int r = k * p.sb + s2;
+                                        vr[r >> 5] |= 1u << (r & 31);
+                                    }
+                            for (int i = 0; i < 4; ++i) ctrl->vrows[st][i] = vr[i];
+                        }
                         if (lane == 0)
                             mbar_arrive_expect_tx(&ctrl->kv_full[st],
                                                   (uint32_t)__popc(mask) * kPP * p.S * 128u);
@@ -701,6 +715,18 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         use = false;
                     }
                     const uint32_t mask = __ballot_sync(0xffffffffu, use);
+                    if (FP8) {
+                        // row r holds a key when its box was loaded and it is before the end
+                        const int key0 = key_base + box0 * p.boxr;
+                        const int boxr_log2 = 31 - __clz(p.boxr);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = 32 * i + lane;
+                            const uint32_t v = __ballot_sync(
+                                0xffffffffu, (mask >> (r >> boxr_log2) & 1u) && key0 + r < x.valid_end);
+                            if (lane == 0) ctrl->vrows[st][i] = v;
+                        }
+                    }
                     if (lane == 0)
                         mbar_arrive_expect_tx(&ctrl->kv_full[st],
                                               (uint32_t)__popc(mask) * kPP * p.boxr * 128u);
@@ -762,7 +788,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 // K/V stage and kv_full parity of the tile S is at, and the stage of the
                 // tile PV is at, kept incrementally (no 64-bit division in this loop)
                 int st_s = 0, st_p = 0;
-                uint32_t par_s = 0;
+                uint32_t par_s = 0, par_p = 0;
                 uint64_t t_idle = 0;
                 uint32_t spins = 0;
                 bool ok = true;
@@ -815,6 +841,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         const int mt = (int)(ip % NUM_MT);
                         const int sb = (int)(ip & 1);
                         bool ready = mbar_test(&ctrl->p_full[sb], (uint32_t)((ip >> 1) & 1));
+                        if (FP8 && ready) ready = mbar_test(&ctrl->cvv_full[st_p], par_p);
                         if (ready && cp.first() && cp.w.seg >= 1)
                             ready = mbar_test(&ctrl->o_empty, (uint32_t)((cp.w.seg - 1) & 1));
                         if (ready) {
@@ -843,7 +870,10 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                 if (cp.last()) umma_commit(&ctrl->o_full);
                                 CPA_TRACE_EVENT(14, gp);
                                 cp.advance(p, ctrl);
-                                if (++st_p == p.n_stages) st_p = 0;
+                                if (++st_p == p.n_stages) {
+                                    st_p = 0;
+                                    par_p ^= 1u;
+                                }
                             }
                             ++ip;
                             progressed = true;
@@ -881,54 +911,69 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             }
             __syncwarp();
         } else if (FP8 && (warp == 2 || warp == 3)) {
-            // ============================== FP8: widening K (warps 2 and 3)
-            // A stage's E4M3 K rows land in the K hi-half region (128 codes = 128 B
-            // per row, 128-B swizzled like every operand row).  Each thread widens
-            // whole rows in place: it reads a row's 128 codes, then writes columns
-            // 0..63 as f16 to the lo-half region and columns 64..127 over the 128 B
-            // it read.  Thread ct owns rows ct and ct + 64; the S MMA waits for
-            // both warps (cv_full).  (V is widened by the softmax warps, before
-            // they need the tile's P: PV waits for them anyway.)  Rows a tile did
-            // not load hold stale data, widened too; their columns are masked.
+            // ============================== FP8 widening (warps 2 and 3)
+            // A stage's E4M3 K and V rows land in the hi-half regions (128 codes =
+            // 128 B per row, 128-B swizzled like every operand row).  Each thread
+            // widens whole rows in place, exactly: it reads a row's 128 codes, then
+            // writes columns 0..63 as f16 to the lo-half region and columns 64..127
+            // over the 128 B it read.  Thread ct owns rows ct and ct + 64 of K (the
+            // S MMA waits for cv_full), then of V (the PV MMA waits for cvv_full).
+            // V rows that hold no key of the sequence (not loaded, or past its end:
+            // stale or arbitrary bytes, NaN codes included) are zeroed instead, so
+            // that P = 0 takes them out exactly; stale K rows are masked columns.
             const int ct = (int)threadIdx.x - 64;
             int st = 0;
             uint32_t par = 0;
             const long long n_tiles = ctrl->count;
             for (long long g = 0; g < n_tiles; ++g) {
-                if (!mbar_wait_warp(&ctrl->kv_full[st], par, abort_flag, p.status)) break;
-                if (ct == 0) CPA_TRACE_EVENT(57, g);
                 uint8_t* stage = smem + p.off_kv + st * kStageBytes;
+                bool okc = true;
 #pragma unroll 1
-                for (int i = 0; i < 2; ++i) {
-                    const int r = ct + 64 * i, sw = r & 7;
-                    uint8_t* lo = stage + r * 128;
-                    uint8_t* hi = lo + kBN * 128;
-                    uint4 c[8];
+                for (int kv = 0; kv < 2 && okc; ++kv) {
+                    if (kv == 0) okc = mbar_wait_warp(&ctrl->kv_full[st], par, abort_flag, p.status);
+                    if (!okc) break;
+                    if (ct == 0 && kv == 0) CPA_TRACE_EVENT(57, g);
+#pragma unroll 1
+                    for (int i = 0; i < 2; ++i) {
+                        const int r = ct + 64 * i, sw = r & 7;
+                        uint8_t* lo = stage + (2 * kv) * (kBN * 128) + r * 128;
+                        uint8_t* hi = lo + kBN * 128;
+                        if (kv == 1 && !(ctrl->vrows[st][r >> 5] >> (r & 31) & 1u)) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        c[j] = *reinterpret_cast<const uint4*>(hi + ((j ^ sw) << 4));
+                            for (int j = 0; j < 8; ++j) {
+                                *reinterpret_cast<uint4*>(lo + (j << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                                *reinterpret_cast<uint4*>(hi + (j << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            continue;
+                        }
+                        uint4 c[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        // codes 16j..16j+15 -> f16 columns 16j..16j+15: 16-B chunks
-                        // 2(j%4) and 2(j%4)+1 of the lo (j < 4) or hi half
-                        uint8_t* row = j < 4 ? lo : hi;
-                        const int ca = 2 * (j & 3);
-                        const uint4 a = make_uint4(e4m3x2_to_f16x2(c[j].x, false),
-                                                   e4m3x2_to_f16x2(c[j].x, true),
-                                                   e4m3x2_to_f16x2(c[j].y, false),
-                                                   e4m3x2_to_f16x2(c[j].y, true));
-                        const uint4 b = make_uint4(e4m3x2_to_f16x2(c[j].z, false),
-                                                   e4m3x2_to_f16x2(c[j].z, true),
-                                                   e4m3x2_to_f16x2(c[j].w, false),
-                                                   e4m3x2_to_f16x2(c[j].w, true));
-                        *reinterpret_cast<uint4*>(row + ((ca ^ sw) << 4)) = a;
-                        *reinterpret_cast<uint4*>(row + (((ca + 1) ^ sw) << 4)) = b;
+                        for (int j = 0; j < 8; ++j)
+                            c[j] = *reinterpret_cast<const uint4*>(hi + ((j ^ sw) << 4));
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            // codes 16j..16j+15 -> f16 columns 16j..16j+15: 16-B chunks
+                            // 2(j%4) and 2(j%4)+1 of the lo (j < 4) or hi half
+                            uint8_t* row = j < 4 ? lo : hi;
+                            const int ca = 2 * (j & 3);
+                            const uint4 a = make_uint4(e4m3x2_to_f16x2(c[j].x, false),
+                                                       e4m3x2_to_f16x2(c[j].x, true),
+                                                       e4m3x2_to_f16x2(c[j].y, false),
+                                                       e4m3x2_to_f16x2(c[j].y, true));
+                            const uint4 b = make_uint4(e4m3x2_to_f16x2(c[j].z, false),
+                                                       e4m3x2_to_f16x2(c[j].z, true),
+                                                       e4m3x2_to_f16x2(c[j].w, false),
+                                                       e4m3x2_to_f16x2(c[j].w, true));
+                            *reinterpret_cast<uint4*>(row + ((ca ^ sw) << 4)) = a;
+                            *reinterpret_cast<uint4*>(row + (((ca + 1) ^ sw) << 4)) = b;
+                        }
                     }
+                    fence_proxy_async_smem();  // the tensor cores read these rows
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(kv == 0 ? &ctrl->cv_full[st] : &ctrl->cvv_full[st]);
+                    if (ct == 0) CPA_TRACE_EVENT(kv == 0 ? 58 : 60, g);
                 }
-                fence_proxy_async_smem();  // the tensor cores read these rows
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctrl->cv_full[st]);
-                if (ct == 0) CPA_TRACE_EVENT(58, g);
+                if (!okc) break;
                 if (++st == p.n_stages) {
                     st = 0;
                     par ^= 1u;
@@ -952,8 +997,6 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
             Walker w;
             w.init(ctrl);
             long long g = 0;
-            int vst = 0;         // FP8: stage of tile g and the parity of its use
-            uint32_t vpar = 0;
             bool ok = true;
             while (w.left > 0 && ok) {
                 const Unit x = get_unit(p, w.u);
@@ -974,48 +1017,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     const int sb = (int)(g % C::kSBufs);
                     const int bi = C::kSBufs == 2 ? sb : mt;
                     const uint32_t par = (uint32_t)((C::kSBufs == 2 ? g >> 1 : g) & 1);
-                    bool okv = true;
-                    if (FP8) {
-                        // widen this tile's V codes (the PV MMA waits for these warps'
-                        // P anyway): thread 2r + hh widens columns 64hh..64hh+63 of V
-                        // row r, in place like the K rows.  The row's two threads are in
-                        // one warp: both read the row's codes before either writes.
-                        okv = mbar_wait_warp(&ctrl->kv_full[vst], vpar, abort_flag, p.status);
-                        if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(59, g);
-                        if (okv) {
-                            const int sidx = (int)threadIdx.x - C::kSmWarp0 * 32;
-                            const int vr = sidx >> 1, hh = sidx & 1, sw = vr & 7;
-                            uint8_t* vlo = smem + p.off_kv + vst * kStageBytes + 2 * kBN * 128 +
-                                           vr * 128;
-                            uint8_t* vhi = vlo + kBN * 128;
-                            uint4 c[4];
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                c[j] = *reinterpret_cast<const uint4*>(vhi + (((4 * hh + j) ^ sw) << 4));
-                            __syncwarp();
-                            uint8_t* row = hh ? vhi : vlo;
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const uint4 a = make_uint4(e4m3x2_to_f16x2_scaled(c[j].x, 0x1404),
-                                                           e4m3x2_to_f16x2_scaled(c[j].x, 0x3424),
-                                                           e4m3x2_to_f16x2_scaled(c[j].y, 0x1404),
-                                                           e4m3x2_to_f16x2_scaled(c[j].y, 0x3424));
-                                const uint4 b = make_uint4(e4m3x2_to_f16x2_scaled(c[j].z, 0x1404),
-                                                           e4m3x2_to_f16x2_scaled(c[j].z, 0x3424),
-                                                           e4m3x2_to_f16x2_scaled(c[j].w, 0x1404),
-                                                           e4m3x2_to_f16x2_scaled(c[j].w, 0x3424));
-                                *reinterpret_cast<uint4*>(row + (((2 * j) ^ sw) << 4)) = a;
-                                *reinterpret_cast<uint4*>(row + (((2 * j + 1) ^ sw) << 4)) = b;
-                            }
-                            fence_proxy_async_smem();  // PV reads these rows
-                        }
-                        if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(60, g);
-                        if (++vst == p.n_stages) {
-                            vst = 0;
-                            vpar ^= 1u;
-                        }
-                    }
-                    bool okl = okv && mbar_wait_warp(&ctrl->s_full[bi], par, abort_flag, p.status);
+                    bool okl = mbar_wait_warp(&ctrl->s_full[bi], par, abort_flag, p.status);
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(4, g);
                     if (lane == 0) CPA_TRACE_EVENT(20 + warp - C::kSmWarp0, g);
                     const bool dtile = jj >= x.n_prefix;
@@ -1206,7 +1208,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(5, g);
                     if (lane == 0) CPA_TRACE_EVENT(44 + warp - C::kSmWarp0, g);
                     bool zeroed = false;
-                    // (FP8: every byte of a page widens to a finite f16, so nothing to clear)
+                    // (FP8: the widening warps zero the V rows that hold no key)
                     if (!FP8 && wgi == 0 && !dtile && key0 + kBN > x.valid_end &&
                         x.valid_end % p.boxr != 0) {
                         // the box holding the sequence's last key was loaded whole: zero
@@ -1356,13 +1358,12 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         oa(blk, f);
                         if (!valid) continue;
                         if (FP8) {
-                            // the widened V carries 2^-8; the V scale is per tensor or
-                            // per (KV head, channel)
+                            // the V scale, per tensor or per (KV head, channel)
                             const float* vs =
                                 p.v_scale + (p.scale_per_channel ? x.h * 128 + blk * 32 : 0);
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
-                                f[e] *= 256.f * __ldg(vs + (p.scale_per_channel ? e : 0));
+                                f[e] *= __ldg(vs + (p.scale_per_channel ? e : 0));
                         }
                         if (fp32_out) {
                             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) +

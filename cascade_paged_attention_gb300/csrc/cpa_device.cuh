@@ -413,24 +413,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// FP8 E4M3 -> f16, scaled by 2^-8, for two codes at a time.  An E4M3 code
-// s.eeee.mmm (exponent bias 7, subnormals at exponent 0) placed with its
-// seven magnitude bits at f16 bits 7..13 and its sign at bit 15 is, read as
-// an f16 (bias 15), exactly its value times 2^-8: normals land on exponent
-// field eeee (so 2^(e-15) = 2^(e-7) * 2^-8) and subnormals on f16
-// subnormals with the same mantissa bits.  Every code maps to a finite f16
-// (the two NaN codes read as +-480 * 2^-8), so stale or garbage bytes can
-// never inject a NaN into the tensor-core operands.
-//   w    four codes (byte 0 = first element)
-//   sel  0x1404: codes 0, 1 -> result; 0x3424: codes 2, 3 -> result
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w, uint32_t sel) {
-    uint32_t t;
-    // each code to the high byte of a 16-bit lane: sign at bit 15, magnitude at 8..14
-    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(w), "r"(sel));
-    const uint32_t u = t >> 1;  // magnitude to bits 7..13, sign to bit 14 (bit 15 is 0)
-    return u + (u & 0x40004000u);  // carry the sign from bit 14 up to bit 15
-}
-
 // FP8 E4M3 -> f16, exact, two codes at a time (the PTX conversion; the NaN
 // codes stay NaN).  `w`: four codes, byte 0 first; `hi` picks codes 2, 3.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w, bool hi) {
