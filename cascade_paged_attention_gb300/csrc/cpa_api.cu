@@ -101,24 +101,22 @@ WsLayout ws_layout(long long n_units, int n_sm) {
     return w;
 }
 
-// Tree verify: the prefix pass's workspace, then its fp32 result.
+// Tree verify: the fused kernel's workspace, then every node's ancestor mask.
 struct TreeWs {
-    size_t attn, o_a, lse_a, total;
+    size_t attn, anc, total;
 };
-TreeWs tree_ws_layout(int B, int N, int H_q, int H_kv, int n_sm) {
+TreeWs tree_ws_layout(int B, int N, int H_kv, int n_sm) {
     TreeWs w;
     w.attn = ws_layout((long long)B * H_kv, n_sm).total;
-    const size_t rows = (size_t)B * N * H_q;
-    w.o_a = w.attn;
-    w.lse_a = align_up(w.o_a + rows * 128 * 4, 256);
-    w.total = align_up(w.lse_a + rows * 4, 256);
+    w.anc = w.attn;
+    w.total = align_up(w.anc + (size_t)B * N * 8, 256);
     return w;
 }
 
 // Multi-level verify: the larger of the two launches' workspaces, then the
-// shared level's and the own level's fp32 partials.
+// shared level's fp32 partial (the own level merges it into its output).
 struct SharedWs {
-    size_t attn, o1, lse1, o2, lse2, total;
+    size_t attn, o1, lse1, total;
 };
 SharedWs shared_ws_layout(int B, int n_groups, int topk, int S, int H_q, int H_kv, int n_sm) {
     SharedWs w;
@@ -132,9 +130,7 @@ SharedWs shared_ws_layout(int B, int n_groups, int topk, int S, int H_q, int H_k
     w.attn = a1 > a2 ? a1 : a2;
     w.o1 = w.attn;
     w.lse1 = align_up(w.o1 + rows * 128 * 4, 256);
-    w.o2 = align_up(w.lse1 + rows * 4, 256);
-    w.lse2 = align_up(w.o2 + rows * 128 * 4, 256);
-    w.total = align_up(w.lse2 + rows * 4, 256);
+    w.total = align_up(w.lse1 + rows * 4, 256);
     return w;
 }
 
@@ -182,7 +178,7 @@ bool plan_geometry(int G, int TS, Geometry& g) {
 // context, so it is raised once per device (and per kernel instance), not once
 // per process: a process that drives several GPUs from one library instance
 // needs it on each of them.
-template <int NUM_MT, bool FP8>
+template <int NUM_MT, int VAR>
 cudaError_t raise_smem_limit_once() {
     static PerDevice<int> state;
     int dev = -1;
@@ -190,19 +186,26 @@ cudaError_t raise_smem_limit_once() {
     if (e != cudaSuccess) return e;
     return (cudaError_t)state.run(dev, (int)cudaErrorInvalidDevice, [](int&) {
         const int optin = smem_optin();
-        return (int)cudaFuncSetAttribute(paged_attn_kernel<NUM_MT, FP8>,
+        return (int)cudaFuncSetAttribute(paged_attn_kernel<NUM_MT, VAR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          optin < kMaxSmemOptin ? optin : kMaxSmemOptin);
     });
 }
 
-template <int NUM_MT, bool FP8>
+template <int NUM_MT, int VAR>
 cudaError_t launch_attn(const AttnParams& p, int smem, int grid, cudaStream_t stream) {
-    cudaError_t e = raise_smem_limit_once<NUM_MT, FP8>();
+    cudaError_t e = raise_smem_limit_once<NUM_MT, VAR>();
     if (e != cudaSuccess) return e;
     if (smem > smem_optin()) return cudaErrorInvalidValue;
-    paged_attn_kernel<NUM_MT, FP8><<<grid, Cfg<NUM_MT>::kThreads, smem, stream>>>(p);
+    paged_attn_kernel<NUM_MT, VAR><<<grid, Cfg<NUM_MT>::kThreads, smem, stream>>>(p);
     return cudaGetLastError();
+}
+
+template <int VAR>
+cudaError_t launch_attn_mt(const AttnParams& p, const Geometry& geo, int grid,
+                           cudaStream_t stream) {
+    return geo.num_mt == 1 ? launch_attn<1, VAR>(p, geo.smem_bytes, grid, stream)
+                           : launch_attn<2, VAR>(p, geo.smem_bytes, grid, stream);
 }
 
 // keep_status: the call is the second launch of one entry point, whose first
@@ -233,9 +236,15 @@ cpa_status run_attn(AttnParams& p, const Geometry& geo, long long n_units, void*
         return CPA_ERR_CUDA;
     // the FP8 instance exists for one M tile only (Q is staged in TMEM as f16)
     if (p.fp8 && geo.num_mt != 1) return CPA_ERR_UNSUPPORTED;
-    cudaError_t e = p.fp8 ? launch_attn<1, true>(p, geo.smem_bytes, n_sm, stream)
-                    : geo.num_mt == 1 ? launch_attn<1, false>(p, geo.smem_bytes, n_sm, stream)
-                                      : launch_attn<2, false>(p, geo.smem_bytes, n_sm, stream);
+    cudaError_t e;
+    if (p.fp8)
+        e = launch_attn<1, VAR_FP8>(p, geo.smem_bytes, n_sm, stream);
+    else if (p.mode == MODE_TREE)
+        e = launch_attn_mt<VAR_TREE>(p, geo, n_sm, stream);
+    else if (p.mrg_o)
+        e = launch_attn_mt<VAR_MERGE>(p, geo, n_sm, stream);
+    else
+        e = launch_attn_mt<VAR_PLAIN>(p, geo, n_sm, stream);
     return e == cudaSuccess ? CPA_OK : CPA_ERR_LAUNCH;
 }
 
@@ -312,13 +321,17 @@ struct Fp8Scales {
 // f32_out: o receives the fp32 result (always for Pass A; for cascade when the
 // result is a partial that a later launch merges).  keep_status: see run_attn.
 // fp8: the pools hold E4M3 codes with these scales (one M tile only).
+// Tree verify (MODE_TREE): dpt is the tree table, S the node count N (topk 1)
+// and anc the nodes' ancestor masks.
 cpa_status verify_common(int mode, const void* q, const void* k_pages, const void* v_pages,
                          const int32_t* ppt, int ppt_stride, const int32_t* dpt, int dpt_stride,
                          const int32_t* lens, int B, int topk, int S, int H_q, int H_kv,
                          int head_dim, int page_size, int num_pages, int max_prefix_len,
                          float sm_scale, void* o, float* lse, void* workspace, size_t ws_bytes,
                          cudaStream_t stream, bool f32_out = false, bool keep_status = false,
-                         const Fp8Scales* fp8 = nullptr) {
+                         const Fp8Scales* fp8 = nullptr,
+                         const unsigned long long* anc = nullptr,
+                         const float* mrg_o = nullptr, const float* mrg_lse = nullptr) {
     cpa_status st = check_verify(q, k_pages, v_pages, ppt, ppt_stride, lens, B, topk, S, H_q, H_kv,
                                  head_dim, page_size, num_pages, max_prefix_len, sm_scale);
     if (st != CPA_OK) return st;
@@ -328,13 +341,17 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
                 (reinterpret_cast<uintptr_t>(fp8->v_scale) & 3u)))
         return CPA_ERR_INVALID_ARG;
     const bool draft = mode != MODE_PASS_A;
+    const bool tree = mode == MODE_TREE;
     // The draft tile holds each branch's drafts in a block of sb rows, all read
-    // from the branch's first draft page.
+    // from the branch's first draft page (tree verify: the tree's nodes in rows
+    // 0..S-1, read through the tree table).
     const int sb = S <= 8 ? 8 : 16;
     const int nbr = mode == MODE_CASCADE ? topk : 1;
     if (draft) {
         if (!dpt || dpt_stride < (S + page_size - 1) / page_size) return CPA_ERR_INVALID_ARG;
-        if (S > kMaxDraft || S > page_size || nbr * sb > kBN) return CPA_ERR_UNSUPPORTED;
+        if (tree ? (S > CPA_MAX_TREE_NODES || !anc || fp8)
+                 : (S > kMaxDraft || S > page_size || nbr * sb > kBN))
+            return CPA_ERR_UNSUPPORTED;
     }
     const int G = H_q / H_kv;
     const int TS = mode == MODE_NAIVE ? S : topk * S;
@@ -356,12 +373,15 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
     p.has_draft = draft ? 1 : 0;
     p.sb = sb;
     p.nbr = nbr;
+    p.anc = anc;
+    p.mrg_o = mrg_o;
+    p.mrg_lse = mrg_lse;
     p.o = o;
     p.lse = lse;
     const uint64_t T = (uint64_t)B * topk * S;
     if (!make_map(&p.qmap, q, H_q, T, G, geo.TSB)) return CPA_ERR_CUDA;
     if (!kv_maps(p, k_pages, v_pages, H_kv, num_pages, page_size)) return CPA_ERR_CUDA;
-    if (draft) {
+    if (draft && !tree) {
         const uint64_t rows = (uint64_t)num_pages * page_size;
         // a branch's draft box is exactly its S rows: the rest of the branch block
         // keeps earlier, finite tile data, which P = 0 there multiplies away
@@ -646,8 +666,6 @@ cpa_status cpa_cascade_verify_shared(const void* q, const void* k_pages, const v
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     float* o1 = reinterpret_cast<float*>(ws + w.o1);
     float* lse1 = reinterpret_cast<float*>(ws + w.lse1);
-    float* o2 = reinterpret_cast<float*>(ws + w.o2);
-    float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
 
     // level 1: the group's draft queries (consecutive tokens) against its shared
     // prefix, read once per group: the rectangle of a prefix-hit prefill whose
@@ -670,17 +688,13 @@ cpa_status cpa_cascade_verify_shared(const void* q, const void* k_pages, const v
     if (!kv_maps(p, k_pages, v_pages, H_kv, num_pages, page_size)) return CPA_ERR_CUDA;
     st = run_attn(p, geo1, (long long)n_groups * H_kv * p.QT, workspace, w.attn, s);
     if (st != CPA_OK) return st;
-    // level 2: own prefix + drafts, the fused cascade kernel, fp32 partial
-    st = verify_common(MODE_CASCADE, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
-                       draft_page_table, draft_pt_stride, prefix_lens, B, topk, S, H_q, H_kv,
-                       head_dim, page_size, num_pages, max_prefix_len, sm_scale, o2, lse2,
-                       workspace, w.attn, s, /*f32_out=*/true, /*keep_status=*/true);
-    if (st != CPA_OK) return st;
-    // level 3: merge
-    const long long rows = (long long)B * topk * S * H_q;
-    return launch_merge_state(o1, lse1, o2, lse2, rows, 128, o, lse, n_sm, s) == cudaSuccess
-               ? CPA_OK
-               : CPA_ERR_LAUNCH;
+    // level 2: own prefix + drafts, the fused cascade kernel, which merges each
+    // finished row with level 1's part of it (the LSE identity) and writes bf16 o
+    return verify_common(MODE_CASCADE, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                         draft_page_table, draft_pt_stride, prefix_lens, B, topk, S, H_q, H_kv,
+                         head_dim, page_size, num_pages, max_prefix_len, sm_scale, o, lse,
+                         workspace, w.attn, s, /*f32_out=*/false, /*keep_status=*/true, nullptr,
+                         nullptr, o1, lse1);
 }
 
 size_t cpa_tree_verify_workspace_size(int B, int N, int H_q, int H_kv, int head_dim,
@@ -690,7 +704,7 @@ size_t cpa_tree_verify_workspace_size(int B, int N, int H_q, int H_kv, int head_
         return 0;
     const int n_sm = sm_count();
     if (n_sm <= 0) return 0;
-    return tree_ws_layout(B, N, H_q, H_kv, n_sm).total;
+    return tree_ws_layout(B, N, H_kv, n_sm).total;
 }
 
 cpa_status cpa_tree_verify(const void* q, const void* k_pages, const void* v_pages,
@@ -700,7 +714,7 @@ cpa_status cpa_tree_verify(const void* q, const void* k_pages, const void* v_pag
                            int H_q, int H_kv, int head_dim, int page_size, int num_pages,
                            int max_prefix_len, float sm_scale, void* o, float* lse,
                            void* workspace, size_t workspace_bytes, cpa_stream_t stream) {
-    // everything checkable is checked before the prefix pass launches
+    // everything checkable is checked before the mask kernel launches
     cpa_status st = check_verify(q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
                                  prefix_lens, B, 1, N, H_q, H_kv, head_dim, page_size, num_pages,
                                  max_prefix_len, sm_scale);
@@ -713,38 +727,25 @@ cpa_status cpa_tree_verify(const void* q, const void* k_pages, const void* v_pag
     if (!plan_geometry(H_q / H_kv, N, geo)) return CPA_ERR_UNSUPPORTED;
     const int n_sm = sm_count();
     if (n_sm <= 0) return CPA_ERR_CUDA;
-    const TreeWs w = tree_ws_layout(B, N, H_q, H_kv, n_sm);
+    const TreeWs w = tree_ws_layout(B, N, H_kv, n_sm);
     if (!workspace || workspace_bytes < w.total) return CPA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CPA_ERR_INVALID_ARG;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    float* o_a = reinterpret_cast<float*>(ws + w.o_a);
-    float* lse_a = reinterpret_cast<float*>(ws + w.lse_a);
+    unsigned long long* anc = reinterpret_cast<unsigned long long*>(ws + w.anc);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // the prefix pass: all N nodes of a request are one query block (topk 1, S N)
-    st = verify_common(MODE_PASS_A, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
-                       nullptr, 0, prefix_lens, B, 1, N, H_q, H_kv, head_dim, page_size,
-                       num_pages, max_prefix_len, sm_scale, o_a, lse_a, workspace, w.attn, s);
-    if (st != CPA_OK) return st;
-    TreeParams tp;
-    tp.q = static_cast<const __nv_bfloat16*>(q);
-    tp.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
-    tp.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
-    tp.ttab = tree_page_table;
-    tp.ttab_stride = tree_pt_stride;
-    tp.parents = tree_parents;
-    tp.B = B;
-    tp.N = N;
-    tp.H_q = H_q;
-    tp.H_kv = H_kv;
-    tp.P = page_size;
-    tp.num_pages = num_pages;
-    tp.scale_log2 = sm_scale * kLog2e;
-    tp.o_a = o_a;
-    tp.lse_a = lse_a;
-    tp.o = o;
-    tp.lse = lse;
-    tp.status = static_cast<uint32_t*>(workspace);
-    return launch_tree(tp, s) == cudaSuccess ? CPA_OK : CPA_ERR_LAUNCH;
+    // the status word first (the mask kernel may set CPA_DEV_BAD_TREE in it),
+    // then every node's ancestor mask, then the fused kernel: the prefix once per
+    // request for all N nodes and the tree as one masked tile of the same online
+    // softmax, merged there
+    if (cudaMemsetAsync(workspace, 0, kStatusBytes, s) != cudaSuccess) return CPA_ERR_CUDA;
+    if (launch_tree_masks(tree_parents, B, N, anc, static_cast<uint32_t*>(workspace), s) !=
+        cudaSuccess)
+        return CPA_ERR_LAUNCH;
+    return verify_common(MODE_TREE, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
+                         tree_page_table, tree_pt_stride, prefix_lens, B, 1, N, H_q, H_kv,
+                         head_dim, page_size, num_pages, max_prefix_len, sm_scale, o, lse,
+                         workspace, w.attn, s, /*f32_out=*/false, /*keep_status=*/true, nullptr,
+                         anc);
 }
 
 cpa_status cpa_tree_pass_b(const void* q, const void* k_pages, const void* v_pages,

@@ -100,10 +100,16 @@ struct AttnParams {
     const __nv_bfloat16* k_pages;
     const __nv_bfloat16* v_pages;
     const int32_t* ptab;  // prefix table (verify) / sequence table (prefill)
-    const int32_t* dtab;  // draft table (verify)
+    const int32_t* dtab;  // draft table (verify) / tree table (tree verify)
+    const unsigned long long* anc;  // tree verify: [B][S] ancestor-or-self masks
     const int32_t* lens;  // prefix lengths (verify)
     void* o;
     float* lse;
+    // when set, every finished row is merged with this partial result of the
+    // same rows (fp32 o [T, H_q, 128], natural-log lse [T, H_q]) by the LSE
+    // identity before it is written (multi-level verify: the shared level)
+    const float* mrg_o;
+    const float* mrg_lse;
     uint32_t* status;
     uint32_t* counters;
     float* part_o;    // [2*n_ctas][kMaxUnitRows][128]
@@ -149,7 +155,9 @@ struct Unit {
     const int32_t* trow;
 };
 
-__device__ __forceinline__ bool is_verify(int mode) { return mode <= MODE_PASS_A; }
+__device__ __forceinline__ bool is_verify(int mode) {
+    return mode <= MODE_PASS_A || mode == MODE_TREE;
+}
 
 __device__ __forceinline__ int prefix_len(const AttnParams& p, int b) {
     int L = __ldg(p.lens + b);
@@ -358,6 +366,10 @@ __device__ __forceinline__ void schedule(const AttnParams& p, Ctrl* c) {
             block_scan(v, c->scan, tot);
             total += tot;
         }
+    } else if (p.mode == MODE_PREFILL_RECT) {
+        // rectangle only: every unit reads the same keys 0..H-1, so units are of
+        // equal size and are split contiguously like verify units
+        total = (long long)p.B * p.H_kv * p.QT * tiles_for(0, p.H_hit);
     } else {
         // Prefill: every q tile of a group (request, KV head) reads the same keys
         // from the start, so the work is dealt so that the CTAs running at any one
@@ -431,6 +443,12 @@ __device__ __forceinline__ void schedule(const AttnParams& p, Ctrl* c) {
             __syncthreads();
             if (c->found) break;
         }
+    } else if (threadIdx.x == 0) {
+        const int tpu = tiles_for(0, p.H_hit);
+        c->u0 = (int)(t0 / tpu);
+        c->j0 = (int)(t0 % tpu);
+        c->ustart = (t0 / tpu) * tpu;
+        c->found = 1;
     }
     __syncthreads();
 }
@@ -508,10 +526,24 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-template <int NUM_MT, bool FP8>
+// Kernel variants.  Each is a separate instance so that the common paths
+// carry no extra code (and no extra registers).
+enum Variant : int {
+    VAR_PLAIN = 0,  // bf16 pools
+    VAR_FP8 = 1,    // FP8 E4M3 pools, widened on chip (one M tile)
+    VAR_TREE = 2,   // tree verify: the unit's last tile holds the draft tree,
+                    // masked per row by ancestor masks
+    VAR_MERGE = 3,  // bf16 pools; every finished row is merged with another
+                    // launch's partial result (p.mrg_o) before it is written
+};
+
+template <int NUM_MT, int VAR>
 __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     paged_attn_kernel(const __grid_constant__ AttnParams p) {
     using C = Cfg<NUM_MT>;
+    constexpr bool FP8 = VAR == VAR_FP8;
+    constexpr bool TREE = VAR == VAR_TREE;
+    constexpr bool MERGE = VAR == VAR_MERGE;
 #ifdef CPA_TRACE
     unsigned long long* const cpa_trace_local = cpa_trace_buf;  // read once
 #endif
@@ -645,7 +677,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 int nxt = load_page(wbase + 32 + lane);
                 // first draft page of branch `lane`, if this piece ends with the draft tile
                 int dpage = -1;
-                if (p.has_draft && je == x.n_tiles && lane < p.nbr)
+                if (!TREE && p.has_draft && je == x.n_tiles && lane < p.nbr)
                     dpage = __ldg(p.dtab + (size_t)(x.b * p.topk + x.branch0 + lane) * p.dtab_stride);
                 for (int jj = jb; jj < je; ++jj, ++g) {
                     // stage st of the ring, used for the (k+1)-th time; its previous use
@@ -661,6 +693,35 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     }
                     if (lane == 0) CPA_TRACE_EVENT(0, g);
                     uint8_t* stage = smem + p.off_kv + st * kStageBytes;
+                    if (TREE && jj >= x.n_prefix) {
+                        // the unit's tree tile: node j (j < S = N) is at logical position j
+                        // of the request's tree table, row j of the tile; box bi = lane
+                        const int32_t* ttab = p.dtab + (size_t)x.b * p.dtab_stride;
+                        const int tpos = lane * p.boxr;
+                        bool use = lane < NB && tpos < p.S;
+                        const int tpg = use ? __ldg(ttab + tpos / p.P) : -1;
+                        if (use && (tpg < 0 || tpg >= p.num_pages)) {
+                            atomicOr(p.status, CPA_DEV_BAD_PAGE);
+                            use = false;
+                        }
+                        const uint32_t mask = __ballot_sync(0xffffffffu, use);
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(&ctrl->kv_full[st],
+                                                  (uint32_t)__popc(mask) * kPP * p.boxr * 128u);
+                        __syncwarp();
+                        for (int t0 = 0; t0 < kPP * NB; t0 += 32) {
+                            const int t = t0 + lane;
+                            const int bi = (t < kPP * NB ? t : 0) / kPP;
+                            const int part = kPP * pi + t % kPP;
+                            const int pgi = __shfl_sync(0xffffffffu, tpg, bi & 31);
+                            if (t < kPP * NB && (mask >> bi & 1u))
+                                tma_load_3d(stage + region(part) * (kBN * 128) + bi * p.boxr * 128,
+                                            part < kParts / 2 ? &p.kmap : &p.vmap, col0(part), x.h,
+                                            pgi * p.P + ((bi * p.boxr) & (p.P - 1)),
+                                            &ctrl->kv_full[st], pol_kv);
+                        }
+                        continue;
+                    }
                     if (jj >= x.n_prefix) {
                         // the unit's draft tile: branch k's drafts 0..S-1 sit in slots
                         // 0..S-1 of its first draft page; copy t = 4k + part loads one
@@ -1012,6 +1073,11 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 // their results stay in their own O rows and are never written.
                 float m_used = neg_inf(), l = 0.f;
                 const bool warp_inert = __all_sync(0xffffffffu, it >= x.ntok);
+                // tree verify: the tree tile's columns this row's node sees (its
+                // ancestors and itself), read once per unit
+                unsigned long long vis = 0ull;
+                if (TREE && it < x.ntok && je == x.n_tiles)
+                    vis = __ldg(p.anc + (size_t)x.b * p.S + it);
                 for (int jj = jb; jj < je; ++jj, ++g) {
                     // this warpgroup's item: S buffer g % 2 (one M tile) or mt (two)
                     const int sb = (int)(g % C::kSBufs);
@@ -1021,6 +1087,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(4, g);
                     if (lane == 0) CPA_TRACE_EVENT(20 + warp - C::kSmWarp0, g);
                     const bool dtile = jj >= x.n_prefix;
+                    const bool tree_tile = TREE && dtile;
                     const int key0 = (x.tile_base + jj) * kBN;
                     // visible columns [lo_c, hi_c) of this tile for this row
                     int lo_c, hi_c;
@@ -1045,11 +1112,27 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     // whole (every row sees all of it) or partial (masked first).  Every tile
                     // runs the same per-piece code, so the rare masked tiles at a unit's end
                     // find it already in the instruction cache; only the masking is extra.
+                    // (the tree tile: the columns of the row's ancestor mask)
+                    auto tree_bits = [&](int a) -> uint32_t {
+                        return a < 64 ? (uint32_t)(vis >> a) : 0u;
+                    };
                     auto piece_class = [&](int a) -> int {  // 0 unseen, 1 partial, 2 whole
+                        if (tree_tile) {
+                            const uint32_t bits = tree_bits(a);
+                            if (!__any_sync(0xffffffffu, bits != 0u)) return 0;
+                            return __all_sync(0xffffffffu, bits == 0xffffffffu) ? 2 : 1;
+                        }
                         if (!__any_sync(0xffffffffu, lo_c < a + 32 && hi_c > a)) return 0;
                         return __all_sync(0xffffffffu, lo_c <= a && hi_c >= a + 32) ? 2 : 1;
                     };
                     auto mask_piece = [&](uint32_t (&v)[32], int a) {
+                        if (tree_tile) {
+                            const uint32_t bits = tree_bits(a);
+#pragma unroll
+                            for (int c = 0; c < 32; ++c)
+                                if (!(bits >> c & 1u)) v[c] = __float_as_uint(neg_inf());
+                            return;
+                        }
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
                             if (a + c < lo_c || a + c >= hi_c) v[c] = __float_as_uint(neg_inf());
@@ -1209,12 +1292,13 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     if (lane == 0) CPA_TRACE_EVENT(44 + warp - C::kSmWarp0, g);
                     bool zeroed = false;
                     // (FP8: the widening warps zero the V rows that hold no key)
-                    if (!FP8 && wgi == 0 && !dtile && key0 + kBN > x.valid_end &&
-                        x.valid_end % p.boxr != 0) {
-                        // the box holding the sequence's last key was loaded whole: zero
-                        // its V rows past the end (whatever the page holds there), so that
-                        // P = 0 contributes exactly nothing
-                        const int first = max(0, x.valid_end - key0);
+                    const bool ztail = dtile ? (tree_tile && p.S % p.boxr != 0)
+                                             : (key0 + kBN > x.valid_end && x.valid_end % p.boxr != 0);
+                    if (!FP8 && wgi == 0 && ztail) {
+                        // the box holding the sequence's last key (or the tree's last node)
+                        // was loaded whole: zero its V rows past the end (whatever the page
+                        // holds there), so that P = 0 contributes exactly nothing
+                        const int first = tree_tile ? p.S : max(0, x.valid_end - key0);
                         const int stop = min(kBN, (first / p.boxr + 1) * p.boxr);
                         const int st = (int)(g % p.n_stages);
                         uint8_t* vb = smem + p.off_kv + st * kStageBytes + 2 * kBN * 128;
@@ -1351,12 +1435,43 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     const int it = R / G, gq = R % G;
                     const bool valid = it < x.ntok;
                     const size_t orow = (size_t)(x.t0 + (valid ? it : 0)) * p.H_q + x.h * G + gq;
+                    // weights of the merge with another level's part (p.mrg_o), log2 units
+                    float mw_own = 1.f, mw_oth = 0.f;
+                    if (MERGE && valid) {
+                        const float lm = __ldg(p.mrg_lse + orow);
+                        const float lo = lm == neg_inf() ? neg_inf() : lm * kLog2e;
+                        if (lse2 == neg_inf() && lo == neg_inf()) {
+                            mw_own = 0.f;
+                        } else {
+                            const float mx = fmaxf(lse2, lo);
+                            const float a = ex2(lse2 - mx), b = ex2(lo - mx);
+                            mw_own = a / (a + b);
+                            mw_oth = b / (a + b);
+                            lse2 = mx + lg2(a + b);
+                        }
+                    }
 #pragma unroll 1
                     for (int blk = 0; blk < 4; ++blk) {
                         float f[32];
                         __syncwarp();
                         oa(blk, f);
                         if (!valid) continue;
+                        if (MERGE) {
+                            // merge with the other level's part of this row:
+                            // o = 2^(lse2 - lm) o_own + 2^(lo - lm) o_other
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) f[e] *= mw_own;
+                            const float4* src =
+                                reinterpret_cast<const float4*>(p.mrg_o + orow * 128 + blk * 32);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float4 v = __ldg(src + e);
+                                f[4 * e] = fmaf(mw_oth, v.x, f[4 * e]);
+                                f[4 * e + 1] = fmaf(mw_oth, v.y, f[4 * e + 1]);
+                                f[4 * e + 2] = fmaf(mw_oth, v.z, f[4 * e + 2]);
+                                f[4 * e + 3] = fmaf(mw_oth, v.w, f[4 * e + 3]);
+                            }
+                        }
                         if (FP8) {
                             // the V scale, per tensor or per (KV head, channel)
                             const float* vs =

@@ -27,6 +27,7 @@ enum Mode : int {
     MODE_PREFILL = 3,       // prefix-hit prefill, rectangle + triangle -> bf16 o
     MODE_PREFILL_RECT = 4,  // rectangle only (keys 0..H-1) -> fp32
     MODE_PREFILL_TRI = 5,   // triangle only (keys H..H+i) -> fp32
+    MODE_TREE = 6,          // Pass A + the draft tree as one masked tile + merge -> bf16 o
 };
 
 // Balanced contiguous split of `total` tiles over `n` CTAs:
