@@ -371,6 +371,78 @@ def prefill_rows(torch, cpa, cpa_synth, timer, dev, peak_tf, iters, cpu):
     return out
 
 
+def next_rows(torch, cpa, cpa_synth, timer, dev, peak, iters, bf16_us):
+    """The built 'next' paths on the pages' example request shape (cold L2):
+    FP8 KV pages, one draft tree per request, a system prompt shared by all."""
+    out = []
+    # FP8 E4M3 pools with per-channel scales
+    wl = cpa_synth.make_verify_fp8(scales="channel", **cpa_synth.VERIFY_CONFIGS[CFG])
+    q = to_device(torch, dev, wl.q, torch.bfloat16)
+    kp, vp = (to_device(torch, dev, a) for a in (wl.k_pages, wl.v_pages))
+    ks, vs = (to_device(torch, dev, np.ascontiguousarray(a, dtype=np.float32))
+              for a in (wl.k_scale, wl.v_scale))
+    ppt, dpt, lens = (to_device(torch, dev, a) for a in (wl.prefix_page_table,
+                                                         wl.draft_page_table, wl.prefix_lens))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[0], wl.H_q, dtype=torch.float32, device=dev)
+
+    def fp8():
+        cpa.cpa_cascade_verify_fp8(q, kp, vp, ks, vs, ppt, dpt, lens, wl.topk, wl.S,
+                                   max_prefix_len=wl.max_prefix_len, o=o, lse=lse)
+
+    st = launch_stats(timer.cold(fp8, iters))
+    b = wl.unique_kv_tokens() * wl.kv_bytes_per_token()
+    out.append({"config": "pages_example, FP8 E4M3 KV pages (per-channel scales)",
+                "unique_kv_bytes": b, "us": st,
+                "gbs": b / (st["median"] * 1e-6) / 1e9,
+                "frac_of_hbm_peak": b / (st["median"] * 1e-6) / 1e9 / peak,
+                "time_vs_bf16_cascade": st["median"] / bf16_us})
+    del q, kp, vp
+    # one 20-node draft tree per request
+    tw = cpa_synth.make_tree_verify(**cpa_synth.TREE_CONFIGS["tree_pages_example"])
+    q, kp, vp = (to_device(torch, dev, a, torch.bfloat16) for a in (tw.q, tw.k_pages, tw.v_pages))
+    ppt, tpt, lens, par = (to_device(torch, dev, a) for a in (
+        tw.prefix_page_table, tw.tree_page_table, tw.prefix_lens, tw.parents))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[0], tw.H_q, dtype=torch.float32, device=dev)
+
+    def tree():
+        cpa.cpa_tree_verify(q, kp, vp, ppt, tpt, lens, par, max_prefix_len=tw.max_prefix_len,
+                            o=o, lse=lse)
+
+    st = launch_stats(timer.cold(tree, iters))
+    b = tw.unique_kv_tokens() * tw.kv_bytes_per_token()
+    out.append({"config": "tree_pages_example: B=64, one 20-node draft tree each, L=2000",
+                "unique_kv_bytes": b, "us": st,
+                "gbs": b / (st["median"] * 1e-6) / 1e9,
+                "frac_of_hbm_peak": b / (st["median"] * 1e-6) / 1e9 / peak,
+                "time_vs_chain_cascade": st["median"] / bf16_us})
+    del q, kp, vp
+    # multi-level: 1024 shared + 976 own prefix tokens
+    sw = cpa_synth.make_shared_verify(**cpa_synth.SHARED_CONFIGS["shared_pages_example"])
+    q, kp, vp = (to_device(torch, dev, a, torch.bfloat16) for a in (sw.q, sw.k_pages, sw.v_pages))
+    spt, ppt, dpt, lens = (to_device(torch, dev, a) for a in (
+        sw.shared_page_table, sw.prefix_page_table, sw.draft_page_table, sw.prefix_lens))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[0], sw.H_q, dtype=torch.float32, device=dev)
+
+    def shared():
+        cpa.cpa_cascade_verify_shared(q, kp, vp, spt, sw.shared_len, ppt, dpt, lens, sw.topk,
+                                      sw.S, max_prefix_len=sw.max_prefix_len, o=o, lse=lse)
+
+    st = launch_stats(timer.cold(shared, iters))
+    b = sw.unique_kv_tokens() * sw.kv_bytes_per_token()
+    out.append({"config": "shared_pages_example: B=64, 1024 shared + 976 own prefix tokens, "
+                          "topk=4, S=5",
+                "unique_kv_bytes": b, "us": st,
+                "gbs": b / (st["median"] * 1e-6) / 1e9,
+                "frac_of_hbm_peak": b / (st["median"] * 1e-6) / 1e9 / peak,
+                "time_vs_single_level_cascade": st["median"] / bf16_us})
+    del q, kp, vp
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -496,6 +568,8 @@ def run_ours(args, world, rank, local):
                                              args.cold_iters, do_cpu, rows_budget=4096))
         configs.extend(prefill_rows(torch, cpa, cpa_synth, timer, dev, peak_tf,
                                     max(5, args.cold_iters // 10), do_cpu))
+        configs.extend(next_rows(torch, cpa, cpa_synth, timer, dev, peak, args.cold_iters,
+                                 cold["median"]))
 
     cpu = None
     if do_cpu:
