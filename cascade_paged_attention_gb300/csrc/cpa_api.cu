@@ -77,9 +77,12 @@ bool make_map_u8(CUtensorMap* map, const void* base, uint64_t dim1, uint64_t dim
     cuuint64_t strides[2] = {128, dim1 * 128};
     cuuint32_t box[3] = {128, box1, box2};
     cuuint32_t estr[3] = {1, 1, 1};
+    // 128-B L2 promotion: a row of one head is 128 B here, and 256-B promotion
+    // (right for bf16, whose 256-B rows are fetched as two halves) would fetch
+    // the neighbouring head's row with every row
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

@@ -855,90 +855,104 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 bool ok = true;
                 while (ip < n_items) {
                     bool progressed = false;
-                    if (is < n_items && is <= ip + 1) {
-                        const long long gs = is / NUM_MT;
-                        const int mt = (int)(is % NUM_MT);
-                        const int qb = p.n_qbufs == 2 ? (cs.w.seg & 1) : 0;
-                        const uint32_t qpar =
-                            (uint32_t)((p.n_qbufs == 2 ? cs.w.seg >> 1 : cs.w.seg) & 1);
-                        const int st = st_s;
-                        const bool q_ready = !cs.first() || mbar_test(&ctrl->q_full[qb], qpar);
-                        if (q_ready && mbar_test(&ready[st], par_s)) {
-                            if (mt == 0) CPA_TRACE_EVENT(2, gs);
-                            tc_fence_after_sync();
-                            const int sb = (int)(is & 1);
-                            const uint32_t kb = sbase + p.off_kv + st * kStageBytes;
-                            const uint32_t qa = sbase + p.off_q + (qb * NUM_MT + mt) * qmt_bytes;
-                            const uint32_t sd = tmem + C::s_col(0, 0) + (uint32_t)sb * 128u;
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const uint64_t bd =
-                                    sdesc_sw128(kb + (kk >> 2) * kBN * 128 + (kk & 3) * 32, 16, 1024);
-                                if (C::kQInTmem) {
-                                    umma_bf16_ts(sd, tmem + C::q_col(qb) + kk * 8, bd, idesc_s,
-                                                 kk > 0 ? 1u : 0u);
-                                } else {
-                                    const uint64_t ad = sdesc_sw128(
-                                        qa + (kk >> 2) * p.Rq * 128 + (kk & 3) * 32, 16, 1024);
-                                    umma_bf16_ss(sd, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                    // With two M tiles, PV of an item is issued before S of the next when
+                    // both are ready (it frees the stage sooner: 442 -> 426 us on the
+                    // long/variable workload); with one M tile S goes first (1 us better)
+                    auto try_s = [&]() {
+                        if (is < n_items && is <= ip + 1) {
+                            const long long gs = is / NUM_MT;
+                            const int mt = (int)(is % NUM_MT);
+                            const int qb = p.n_qbufs == 2 ? (cs.w.seg & 1) : 0;
+                            const uint32_t qpar =
+                                (uint32_t)((p.n_qbufs == 2 ? cs.w.seg >> 1 : cs.w.seg) & 1);
+                            const int st = st_s;
+                            const bool q_ready = !cs.first() || mbar_test(&ctrl->q_full[qb], qpar);
+                            if (q_ready && mbar_test(&ready[st], par_s)) {
+                                if (mt == 0) CPA_TRACE_EVENT(2, gs);
+                                tc_fence_after_sync();
+                                const int sb = (int)(is & 1);
+                                const uint32_t kb = sbase + p.off_kv + st * kStageBytes;
+                                const uint32_t qa = sbase + p.off_q + (qb * NUM_MT + mt) * qmt_bytes;
+                                const uint32_t sd = tmem + C::s_col(0, 0) + (uint32_t)sb * 128u;
+    #pragma unroll
+                                for (int kk = 0; kk < 8; ++kk) {
+                                    const uint64_t bd =
+                                        sdesc_sw128(kb + (kk >> 2) * kBN * 128 + (kk & 3) * 32, 16, 1024);
+                                    if (C::kQInTmem) {
+                                        umma_bf16_ts(sd, tmem + C::q_col(qb) + kk * 8, bd, idesc_s,
+                                                     kk > 0 ? 1u : 0u);
+                                    } else {
+                                        const uint64_t ad = sdesc_sw128(
+                                            qa + (kk >> 2) * p.Rq * 128 + (kk & 3) * 32, 16, 1024);
+                                        umma_bf16_ss(sd, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                                    }
                                 }
-                            }
-                            umma_commit(&ctrl->s_full[sb]);
-                            if (mt == NUM_MT - 1) {
-                                if (cs.last()) umma_commit(&ctrl->q_empty[qb]);
-                                CPA_TRACE_EVENT(15, gs);
-                                cs.advance(p, ctrl);
-                                if (++st_s == p.n_stages) {
-                                    st_s = 0;
-                                    par_s ^= 1u;
+                                umma_commit(&ctrl->s_full[sb]);
+                                if (mt == NUM_MT - 1) {
+                                    if (cs.last()) umma_commit(&ctrl->q_empty[qb]);
+                                    CPA_TRACE_EVENT(15, gs);
+                                    cs.advance(p, ctrl);
+                                    if (++st_s == p.n_stages) {
+                                        st_s = 0;
+                                        par_s ^= 1u;
+                                    }
                                 }
+                                ++is;
+                                progressed = true;
                             }
-                            ++is;
-                            progressed = true;
                         }
-                    }
-                    if (ip < is) {
-                        const long long gp = ip / NUM_MT;
-                        const int mt = (int)(ip % NUM_MT);
-                        const int sb = (int)(ip & 1);
-                        bool ready = mbar_test(&ctrl->p_full[sb], (uint32_t)((ip >> 1) & 1));
-                        if (FP8 && ready) ready = mbar_test(&ctrl->cvv_full[st_p], par_p);
-                        if (ready && cp.first() && cp.w.seg >= 1)
-                            ready = mbar_test(&ctrl->o_empty, (uint32_t)((cp.w.seg - 1) & 1));
-                        if (ready) {
-                            if (mt == 0) CPA_TRACE_EVENT(3, gp);
-                            tc_fence_after_sync();
-                            const int st = st_p;
-                            const uint32_t vb = sbase + p.off_kv + st * kStageBytes + 2 * kBN * 128;
-                            const bool first = cp.first();
-                            const int passes = cp.jj == cp.x.resid_tile ? 2 : 1;
-                            // P of keys 64c..64c+63 (bf16, two per column) sits in the
-                            // first 32 of the 64 S columns those keys came from, its
-                            // residual in the other 32
-                            const uint32_t pa = tmem + C::s_col(0, 0) + (uint32_t)sb * 128u;
-                            for (int pass = 0; pass < passes; ++pass) {
-#pragma unroll
-                                for (int kk = 0; kk < kBN / 16; ++kk) {
-                                    const uint64_t bd = sdesc_sw128(vb + kk * 16 * 128, kBN * 128, 1024);
-                                    umma_bf16_ts(tmem + C::o_col(mt),
-                                                 pa + (kk >> 2) * 64 + pass * 32 + (kk & 3) * 8, bd,
-                                                 idesc_o, (first && pass == 0 && kk == 0) ? 0u : 1u);
+                    };
+                    auto try_pv = [&]() {
+                        if (ip < is) {
+                            const long long gp = ip / NUM_MT;
+                            const int mt = (int)(ip % NUM_MT);
+                            const int sb = (int)(ip & 1);
+                            bool ready = mbar_test(&ctrl->p_full[sb], (uint32_t)((ip >> 1) & 1));
+                            if (FP8 && ready) ready = mbar_test(&ctrl->cvv_full[st_p], par_p);
+                            if (ready && cp.first() && cp.w.seg >= 1)
+                                ready = mbar_test(&ctrl->o_empty, (uint32_t)((cp.w.seg - 1) & 1));
+                            if (ready) {
+                                if (mt == 0) CPA_TRACE_EVENT(3, gp);
+                                tc_fence_after_sync();
+                                const int st = st_p;
+                                const uint32_t vb = sbase + p.off_kv + st * kStageBytes + 2 * kBN * 128;
+                                const bool first = cp.first();
+                                const int passes = cp.jj == cp.x.resid_tile ? 2 : 1;
+                                // P of keys 64c..64c+63 (bf16, two per column) sits in the
+                                // first 32 of the 64 S columns those keys came from, its
+                                // residual in the other 32
+                                const uint32_t pa = tmem + C::s_col(0, 0) + (uint32_t)sb * 128u;
+                                for (int pass = 0; pass < passes; ++pass) {
+    #pragma unroll
+                                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                                        const uint64_t bd = sdesc_sw128(vb + kk * 16 * 128, kBN * 128, 1024);
+                                        umma_bf16_ts(tmem + C::o_col(mt),
+                                                     pa + (kk >> 2) * 64 + pass * 32 + (kk & 3) * 8, bd,
+                                                     idesc_o, (first && pass == 0 && kk == 0) ? 0u : 1u);
+                                    }
                                 }
-                            }
-                            umma_commit(&ctrl->p_empty[sb]);
-                            if (mt == NUM_MT - 1) {
-                                umma_commit(&ctrl->kv_empty[st]);
-                                if (cp.last()) umma_commit(&ctrl->o_full);
-                                CPA_TRACE_EVENT(14, gp);
-                                cp.advance(p, ctrl);
-                                if (++st_p == p.n_stages) {
-                                    st_p = 0;
-                                    par_p ^= 1u;
+                                umma_commit(&ctrl->p_empty[sb]);
+                                if (mt == NUM_MT - 1) {
+                                    umma_commit(&ctrl->kv_empty[st]);
+                                    if (cp.last()) umma_commit(&ctrl->o_full);
+                                    CPA_TRACE_EVENT(14, gp);
+                                    cp.advance(p, ctrl);
+                                    if (++st_p == p.n_stages) {
+                                        st_p = 0;
+                                        par_p ^= 1u;
+                                    }
                                 }
+                                ++ip;
+                                progressed = true;
                             }
-                            ++ip;
-                            progressed = true;
                         }
+                    };
+                    if (NUM_MT == 2) {
+                        try_pv();
+                        try_s();
+                    } else {
+                        try_s();
+                        try_pv();
                     }
                     if (progressed) {
                         spins = 0;
@@ -1000,10 +1014,12 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         uint8_t* lo = stage + (2 * kv) * (kBN * 128) + r * 128;
                         uint8_t* hi = lo + kBN * 128;
                         if (kv == 1 && !(ctrl->vrows[st][r >> 5] >> (r & 31) & 1u)) {
+                            // (chunks in swizzled order, like every other access: the
+                            // rows of 8 neighbouring lanes then fall in distinct banks)
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
-                                *reinterpret_cast<uint4*>(lo + (j << 4)) = make_uint4(0u, 0u, 0u, 0u);
-                                *reinterpret_cast<uint4*>(hi + (j << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                                *reinterpret_cast<uint4*>(lo + ((j ^ sw) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                                *reinterpret_cast<uint4*>(hi + ((j ^ sw) << 4)) = make_uint4(0u, 0u, 0u, 0u);
                             }
                             continue;
                         }
