@@ -104,16 +104,10 @@ WsLayout ws_layout(long long n_units, int n_sm) {
     return w;
 }
 
-// Tree verify: the fused kernel's workspace, then every node's ancestor mask.
-struct TreeWs {
-    size_t attn, anc, total;
-};
-TreeWs tree_ws_layout(int B, int N, int H_kv, int n_sm) {
-    TreeWs w;
-    w.attn = ws_layout((long long)B * H_kv, n_sm).total;
-    w.anc = w.attn;
-    w.total = align_up(w.anc + (size_t)B * N * 8, 256);
-    return w;
+// Tree verify: the fused kernel's workspace (the kernel builds the ancestor
+// masks itself, from the parent array).
+size_t tree_ws_bytes(int B, int H_kv, int n_sm) {
+    return ws_layout((long long)B * H_kv, n_sm).total;
 }
 
 // Multi-level verify: the larger of the two launches' workspaces, then the
@@ -325,7 +319,7 @@ struct Fp8Scales {
 // result is a partial that a later launch merges).  keep_status: see run_attn.
 // fp8: the pools hold E4M3 codes with these scales (one M tile only).
 // Tree verify (MODE_TREE): dpt is the tree table, S the node count N (topk 1)
-// and anc the nodes' ancestor masks.
+// and tree_par the parent array [B][N].
 cpa_status verify_common(int mode, const void* q, const void* k_pages, const void* v_pages,
                          const int32_t* ppt, int ppt_stride, const int32_t* dpt, int dpt_stride,
                          const int32_t* lens, int B, int topk, int S, int H_q, int H_kv,
@@ -333,7 +327,7 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
                          float sm_scale, void* o, float* lse, void* workspace, size_t ws_bytes,
                          cudaStream_t stream, bool f32_out = false, bool keep_status = false,
                          const Fp8Scales* fp8 = nullptr,
-                         const unsigned long long* anc = nullptr,
+                         const int32_t* tree_par = nullptr,
                          const float* mrg_o = nullptr, const float* mrg_lse = nullptr) {
     cpa_status st = check_verify(q, k_pages, v_pages, ppt, ppt_stride, lens, B, topk, S, H_q, H_kv,
                                  head_dim, page_size, num_pages, max_prefix_len, sm_scale);
@@ -352,7 +346,7 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
     const int nbr = mode == MODE_CASCADE ? topk : 1;
     if (draft) {
         if (!dpt || dpt_stride < (S + page_size - 1) / page_size) return CPA_ERR_INVALID_ARG;
-        if (tree ? (S > CPA_MAX_TREE_NODES || !anc || fp8)
+        if (tree ? (S > CPA_MAX_TREE_NODES || !tree_par || fp8)
                  : (S > kMaxDraft || S > page_size || nbr * sb > kBN))
             return CPA_ERR_UNSUPPORTED;
     }
@@ -376,7 +370,7 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
     p.has_draft = draft ? 1 : 0;
     p.sb = sb;
     p.nbr = nbr;
-    p.anc = anc;
+    p.tree_par = tree_par;
     p.mrg_o = mrg_o;
     p.mrg_lse = mrg_lse;
     p.o = o;
@@ -707,7 +701,7 @@ size_t cpa_tree_verify_workspace_size(int B, int N, int H_q, int H_kv, int head_
         return 0;
     const int n_sm = sm_count();
     if (n_sm <= 0) return 0;
-    return tree_ws_layout(B, N, H_kv, n_sm).total;
+    return tree_ws_bytes(B, H_kv, n_sm);
 }
 
 cpa_status cpa_tree_verify(const void* q, const void* k_pages, const void* v_pages,
@@ -730,25 +724,15 @@ cpa_status cpa_tree_verify(const void* q, const void* k_pages, const void* v_pag
     if (!plan_geometry(H_q / H_kv, N, geo)) return CPA_ERR_UNSUPPORTED;
     const int n_sm = sm_count();
     if (n_sm <= 0) return CPA_ERR_CUDA;
-    const TreeWs w = tree_ws_layout(B, N, H_kv, n_sm);
-    if (!workspace || workspace_bytes < w.total) return CPA_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CPA_ERR_INVALID_ARG;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    unsigned long long* anc = reinterpret_cast<unsigned long long*>(ws + w.anc);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // the status word first (the mask kernel may set CPA_DEV_BAD_TREE in it),
-    // then every node's ancestor mask, then the fused kernel: the prefix once per
-    // request for all N nodes and the tree as one masked tile of the same online
-    // softmax, merged there
-    if (cudaMemsetAsync(workspace, 0, kStatusBytes, s) != cudaSuccess) return CPA_ERR_CUDA;
-    if (launch_tree_masks(tree_parents, B, N, anc, static_cast<uint32_t*>(workspace), s) !=
-        cudaSuccess)
-        return CPA_ERR_LAUNCH;
+    if (!workspace || workspace_bytes < tree_ws_bytes(B, H_kv, n_sm)) return CPA_ERR_WORKSPACE;
+    // one launch: the prefix once per request for all N nodes and the tree as one
+    // more tile of the same online softmax, masked per row by the node's ancestor
+    // mask (built in the kernel from the parent array), merged there
     return verify_common(MODE_TREE, q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
                          tree_page_table, tree_pt_stride, prefix_lens, B, 1, N, H_q, H_kv,
                          head_dim, page_size, num_pages, max_prefix_len, sm_scale, o, lse,
-                         workspace, w.attn, s, /*f32_out=*/false, /*keep_status=*/true, nullptr,
-                         anc);
+                         workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
+                         /*f32_out=*/false, /*keep_status=*/false, nullptr, tree_parents);
 }
 
 cpa_status cpa_tree_pass_b(const void* q, const void* k_pages, const void* v_pages,

@@ -101,7 +101,7 @@ struct AttnParams {
     const __nv_bfloat16* v_pages;
     const int32_t* ptab;  // prefix table (verify) / sequence table (prefill)
     const int32_t* dtab;  // draft table (verify) / tree table (tree verify)
-    const unsigned long long* anc;  // tree verify: [B][S] ancestor-or-self masks
+    const int32_t* tree_par;  // tree verify: [B][S] parent index of every node (-1: a root)
     const int32_t* lens;  // prefix lengths (verify)
     void* o;
     float* lse;
@@ -1089,11 +1089,40 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 // their results stay in their own O rows and are never written.
                 float m_used = neg_inf(), l = 0.f;
                 const bool warp_inert = __all_sync(0xffffffffu, it >= x.ntok);
-                // tree verify: the tree tile's columns this row's node sees (its
-                // ancestors and itself), read once per unit
+                // tree verify: the tree tile's columns this row's node sees, its
+                // ancestor-or-self mask (tutorial section 8.2: M[i, j] = 1 iff j is in
+                // A(i)).  Every warp holds the request's parent array in registers
+                // (lane l: parents l and l + 32) and each thread climbs its own node's
+                // chain with warp shuffles (at most N steps, each to a smaller index;
+                // an index outside [-1, i) stops the climb and sets CPA_DEV_BAD_TREE).
+                // Warp-local, so no barrier across warps; done once per unit, before
+                // its first tile.
                 unsigned long long vis = 0ull;
-                if (TREE && it < x.ntok && je == x.n_tiles)
-                    vis = __ldg(p.anc + (size_t)x.b * p.S + it);
+                if (TREE && je == x.n_tiles) {
+                    const int32_t* tpar = p.tree_par + (size_t)x.b * p.S;
+                    const int tpar_lo = lane < p.S ? __ldg(tpar + lane) : -1;
+                    const int tpar_hi = lane + 32 < p.S ? __ldg(tpar + lane + 32) : -1;
+                    bool act = it < x.ntok;
+                    int j = it;
+                    vis = act ? 1ull << it : 0ull;
+                    for (int step = 0; step < p.S; ++step) {
+                        if (!__any_sync(0xffffffffu, act)) break;
+                        const int a = __shfl_sync(0xffffffffu, tpar_lo, j & 31);
+                        const int b = __shfl_sync(0xffffffffu, tpar_hi, j & 31);
+                        const int pj = j < 32 ? a : b;
+                        if (act) {
+                            if (pj == -1) {
+                                act = false;
+                            } else if (pj < -1 || pj >= j) {
+                                atomicOr(p.status, CPA_DEV_BAD_TREE);
+                                act = false;
+                            } else {
+                                vis |= 1ull << pj;
+                                j = pj;
+                            }
+                        }
+                    }
+                }
                 for (int jj = jb; jj < je; ++jj, ++g) {
                     // this warpgroup's item: S buffer g % 2 (one M tile) or mt (two)
                     const int sb = (int)(g % C::kSBufs);

@@ -125,36 +125,6 @@ __global__ void __launch_bounds__(256) pass_b_kernel(PassBParams p) {
 // the cascade page and writes bf16 o; otherwise it writes its own fp32 part.
 constexpr int kTreeHeadsPerWarp = 4;
 
-// Ancestor-or-self masks of every node of every request's draft tree, for the
-// tree tile of the fused verify kernel: bit j of anc[b*N + i] is set iff node j
-// is node i or one of its ancestors (tutorial section 8.2: M[i, j] = 1 iff j is
-// in A(i)).  One thread per node climbs the parent chain (each step moves to a
-// smaller index, so at most N steps); a parent index outside [-1, i) stops the
-// climb and sets CPA_DEV_BAD_TREE.
-__global__ void __launch_bounds__(256) tree_masks_kernel(const int32_t* __restrict__ parents,
-                                                         int B, int N,
-                                                         unsigned long long* __restrict__ anc,
-                                                         uint32_t* status) {
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= B * N) return;
-    const int b = t / N, i = t % N;
-    const int32_t* par = parents + (size_t)b * N;
-    unsigned long long m = 1ull << i;
-    bool bad = false;
-    for (int j = i, step = 0; step < N; ++step) {
-        const int pj = __ldg(par + j);
-        if (pj == -1) break;
-        if (pj < -1 || pj >= j) {
-            bad = true;
-            break;
-        }
-        m |= 1ull << pj;
-        j = pj;
-    }
-    if (bad) atomicOr(status, CPA_DEV_BAD_TREE);
-    anc[t] = m;
-}
-
 __global__ void __launch_bounds__(256) tree_kernel(TreeParams p) {
     __shared__ __align__(16) __nv_bfloat16 ks[CPA_MAX_TREE_NODES][128];
     __shared__ __align__(16) __nv_bfloat16 vs[CPA_MAX_TREE_NODES][128];
@@ -333,13 +303,6 @@ cudaError_t launch_pass_b(const PassBParams& p, cudaStream_t stream) {
 cudaError_t launch_tree(const TreeParams& p, cudaStream_t stream) {
     const long long blocks = (long long)p.B * p.H_kv;
     tree_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_tree_masks(const int32_t* parents, int B, int N, unsigned long long* anc,
-                              uint32_t* status, cudaStream_t stream) {
-    const int n = B * N;
-    tree_masks_kernel<<<(n + 255) / 256, 256, 0, stream>>>(parents, B, N, anc, status);
     return cudaGetLastError();
 }
 

@@ -45,8 +45,6 @@ cudaError_t launch_merge_state(const float* o_a, const float* lse_a, const float
                                float* lse_out, int n_sm, cudaStream_t stream);
 cudaError_t launch_pass_b(const PassBParams& p, cudaStream_t stream);
 cudaError_t launch_tree(const TreeParams& p, cudaStream_t stream);
-cudaError_t launch_tree_masks(const int32_t* parents, int B, int N, unsigned long long* anc,
-                              uint32_t* status, cudaStream_t stream);
 cudaError_t launch_wait_timeout(uint32_t* status, unsigned long long limit_ns,
                                 cudaStream_t stream);
 

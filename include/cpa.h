@@ -316,9 +316,8 @@ cpa_status cpa_cascade_verify_shared(const void* q, const void* k_pages, const v
 
 /*
  * Bytes of workspace cpa_tree_verify needs for these sizes on the current
- * device (0 for sizes it would reject).  Besides the status word and the
- * merge scratch of the attention kernel it holds every node's 64-bit
- * ancestor mask, B*N*8 bytes.
+ * device (0 for sizes it would reject): the status word and the merge
+ * scratch of the attention kernel.
  */
 size_t cpa_tree_verify_workspace_size(int B, int N, int H_q, int H_kv, int head_dim,
                                       int page_size);
@@ -330,12 +329,11 @@ size_t cpa_tree_verify_workspace_size(int B, int N, int H_q, int H_kv, int head_
  * its children (BFS order does).  Node i attends the whole prefix and the
  * tree nodes of A(i), its ancestors and itself: the mask M[i, j] = 1 iff j is
  * in A(i), the tree generalisation of the causal mask.  The chain-per-branch
- * case of cpa_cascade_verify is the forest of topk chains.  Two launches: a
- * small kernel builds every node's ancestor mask from the parent array, then
- * the tensor-core kernel reads the prefix once per request for all N nodes
- * (the cascade page's Pass A) and takes the N tree nodes as one more tile of
- * the same online softmax, masked per row by the node's ancestor mask, so the
- * two parts are merged there.
+ * case of cpa_cascade_verify is the forest of topk chains.  One launch: the
+ * tensor-core kernel reads the prefix once per request for all N nodes (the
+ * cascade page's Pass A) and takes the N tree nodes as one more tile of the
+ * same online softmax, masked per row by the node's ancestor mask (built on
+ * chip from the parent array), so the two parts are merged there.
  *   q                  bf16 [B*N, H_q, head_dim]; token b*N + i is node i of
  *                      request b.
  *   tree_page_table    int32 [B, tree_pt_stride]: node j of request b's tree
