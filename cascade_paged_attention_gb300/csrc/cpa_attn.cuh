@@ -22,7 +22,9 @@
 //              ahead by the whole warp) and issues TMA loads of 128-B
 //              swizzled K/V boxes (one copy per lane) into a ring of 128-key
 //              stages; for units of two M tiles it also loads Q by TMA;
-//   w = 1      MMA issuer: S = Q K^T (M=128, N=128, K=128) into TMEM, then
+//   w = 2      (bf16) producer of the V halves, beside warp 0's K halves;
+//   w = 3      MMA issuer (FP8 instance: w = 1, and w = 2, 3 widen the E4M3
+//              rows to f16): S = Q K^T (M=128, N=128, K=128) into TMEM, then
 //              O += P V (M=128, N=128, K=128) into TMEM.  With one M tile Q
 //              sits in TMEM and both MMAs read their A operand from there;
 //   w = 4..11  softmax: two warpgroups.  With one M tile they split each
@@ -556,6 +558,12 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     float* xsum = reinterpret_cast<float*>(smem + kOffSum);
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The thread that issues the MMAs shares its SMSP (warp % 4) with the two
+    // softmax warps of TMEM lanes 32 (warp % 4) .. +31.  Warp 3 puts it beside
+    // the warps of rows 96..127, which have nothing to do in units of up to 96
+    // rows (the verify shapes): 1-2 % faster there than beside rows 32..63.  The
+    // FP8 instance widens on warps 2 and 3 and issues from warp 1.
+    constexpr int kMmaWarp = FP8 ? 1 : 3;
     volatile uint32_t* abort_flag = &ctrl->abort_flag;
 
     if (threadIdx.x == 0) {
@@ -821,7 +829,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                               p.status);
                 }
             }
-        } else if (warp == 1) {
+        } else if (warp == kMmaWarp) {
             // ============================== MMA issuer
             // The work is a sequence of items, one per (tile, M tile): item i uses S
             // buffer i % 2 (one M tile: consecutive tiles alternate between two S
