@@ -962,18 +962,10 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         try_s();
                         try_pv();
                     }
-                    if (progressed) {
-                        spins = 0;
-                    } else {
-                        // Nothing ready: suspend on the barrier that gates the next PV
-                        // (it frees a K/V stage), or on the next K/V tile when no PV is
-                        // pending.  The thread wakes when the phase completes; the hint
-                        // bounds the wait so the other barrier is re-checked.
-                        if (ip < is)
-                            mbar_try_wait_hint(&ctrl->p_full[ip & 1], (uint32_t)((ip >> 1) & 1), 200);
-                        else if (is < n_items)
-                            mbar_try_wait_hint(&ready[st_s], par_s, 200);
-                    }
+                    // Nothing ready: poll again.  (Suspending on the barrier that gates
+                    // the next item, with a 0-200 ns hint or a 32-100 ns sleep, woke no
+                    // sooner and cost the Llama-shaped call about 1 %.)
+                    if (progressed) spins = 0;
                     if (!progressed && (++spins & 63u) == 0) {
                         // same time limit as every other wait of the kernel
                         const uint64_t now = globaltimer_ns();

@@ -71,20 +71,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Suspend until the phase completes or about `hint_ns` passes; true if it completed.
-__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
-                                                   uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
 // Bounded wait for the phase with the given parity to complete.
 // Returns false (and the CTA is in abort mode) if the wait gave up or another
 // role of the CTA already gave up.
