@@ -294,7 +294,7 @@ def verify_config_row(torch, cpa, cpa_synth, timer, dev, name, peak, iters, cpu,
 
     unique = wl.unique_kv_tokens() * wl.kv_bytes_per_token()
     c = launch_stats(timer.cold(cascade, iters))
-    n = launch_stats(timer.cold(naive, max(5, iters // 4)))
+    n = launch_stats(timer.cold(naive, max(50, iters // 2)))
     row = {
         "config": name, "unique_kv_bytes": unique,
         "naive_kv_bytes": wl.naive_kv_tokens() * wl.kv_bytes_per_token(),
@@ -521,7 +521,7 @@ def run_ours(args, world, rank, local):
 
     # the same call with L2 flushed before every launch (cold-L2 figure)
     cold = launch_stats(timer.cold(cascade, args.cold_iters))
-    cold_naive = launch_stats(timer.cold(naive, max(5, args.cold_iters // 4)))
+    cold_naive = launch_stats(timer.cold(naive, max(50, args.cold_iters // 2)))
 
     # end to end through the public API: host inputs -> device, call, result -> host.
     # The two KV pools go up on two streams at once (one copy stream does not fill
@@ -567,7 +567,7 @@ def run_ours(args, world, rank, local):
             configs.append(verify_config_row(torch, cpa, cpa_synth, timer, dev, name, peak,
                                              args.cold_iters, do_cpu, rows_budget=4096))
         configs.extend(prefill_rows(torch, cpa, cpa_synth, timer, dev, peak_tf,
-                                    max(5, args.cold_iters // 10), do_cpu))
+                                    max(50, args.cold_iters // 2), do_cpu))
         configs.extend(next_rows(torch, cpa, cpa_synth, timer, dev, peak, args.cold_iters,
                                  cold["median"]))
 
