@@ -289,6 +289,7 @@ void fill_common(AttnParams& p, const void* q, const void* k_pages, const void* 
     p.P = page_size;
     p.num_pages = num_pages;
     p.max_len = max_prefix_len;
+    p.s_grp = 1;
     p.boxr = page_size < kBN ? page_size : kBN;
     p.scale_log2 = sm_scale * kLog2e;
 }
@@ -317,6 +318,14 @@ struct Fp8Scales {
 
 // f32_out: o receives the fp32 result (always for Pass A; for cascade when the
 // result is a partial that a later launch merges).  keep_status: see run_attn.
+// A prefix segment shared by groups of `grp` consecutive requests: `len`
+// logical positions (whole pages) read through row b / grp of `table`, before
+// each request's own prefix.
+struct SharedSeg {
+    const int32_t* table;
+    int stride, len, grp;
+};
+
 // fp8: the pools hold E4M3 codes with these scales (one M tile only).
 // Tree verify (MODE_TREE): dpt is the tree table, S the node count N (topk 1)
 // and tree_par the parent array [B][N].
@@ -328,7 +337,8 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
                          cudaStream_t stream, bool f32_out = false, bool keep_status = false,
                          const Fp8Scales* fp8 = nullptr,
                          const int32_t* tree_par = nullptr,
-                         const float* mrg_o = nullptr, const float* mrg_lse = nullptr) {
+                         const float* mrg_o = nullptr, const float* mrg_lse = nullptr,
+                         const SharedSeg* seg = nullptr) {
     cpa_status st = check_verify(q, k_pages, v_pages, ppt, ppt_stride, lens, B, topk, S, H_q, H_kv,
                                  head_dim, page_size, num_pages, max_prefix_len, sm_scale);
     if (st != CPA_OK) return st;
@@ -371,6 +381,12 @@ cpa_status verify_common(int mode, const void* q, const void* k_pages, const voi
     p.sb = sb;
     p.nbr = nbr;
     p.tree_par = tree_par;
+    if (seg) {
+        p.stab = seg->table;
+        p.stab_stride = seg->stride;
+        p.s_len = seg->len;
+        p.s_grp = seg->grp;
+    }
     p.mrg_o = mrg_o;
     p.mrg_lse = mrg_lse;
     p.o = o;
@@ -651,6 +667,22 @@ cpa_status cpa_cascade_verify_shared(const void* q, const void* k_pages, const v
     if (!draft_page_table || draft_pt_stride < (S + page_size - 1) / page_size)
         return CPA_ERR_INVALID_ARG;
     if (S > kMaxDraft || S > page_size || topk * sb > kBN) return CPA_ERR_UNSUPPORTED;
+    if (shared_len % page_size == 0) {
+        // A whole number of shared pages: one launch.  Every (request, KV head)
+        // unit walks its group's shared pages, then its own, then its drafts;
+        // the requests of a group read the shared pages at about the same time,
+        // so DRAM delivers them once and L2 serves the rest.  The kernel is
+        // bound by per-tile work rather than by bytes, and this schedule has
+        // the tiles of a single-level call, without the first level's short
+        // units, its fp32 partial and a second launch.
+        const SharedSeg seg{shared_page_table, shared_pt_stride, shared_len, B / n_groups};
+        return verify_common(MODE_CASCADE, q, k_pages, v_pages, prefix_page_table,
+                             prefix_pt_stride, draft_page_table, draft_pt_stride, prefix_lens, B,
+                             topk, S, H_q, H_kv, head_dim, page_size, num_pages, max_prefix_len,
+                             sm_scale, o, lse, workspace, workspace_bytes, s, false, false,
+                             nullptr, nullptr, nullptr, nullptr, &seg);
+    }
+    // Otherwise two launches (the shared prefix ends inside a page).
     const int G = H_q / H_kv;
     Geometry geo1, geo2;
     if (!plan_geometry(G, 128 / G, geo1) || !plan_geometry(G, topk * S, geo2))

@@ -105,6 +105,13 @@ struct AttnParams {
     const int32_t* dtab;  // draft table (verify) / tree table (tree verify)
     const int32_t* tree_par;  // tree verify: [B][S] parent index of every node (-1: a root)
     const int32_t* lens;  // prefix lengths (verify)
+    // verify over a prefix shared by groups of s_grp consecutive requests: the
+    // first s_len logical positions (a whole number of pages) of request b are
+    // the shared prefix of its group, read through row b / s_grp of stab; the
+    // request's own prefix (lens[b] tokens, table ptab) follows it.  s_len = 0:
+    // no shared segment.
+    const int32_t* stab;
+    int stab_stride, s_len, s_grp;
     void* o;
     float* lse;
     // when set, every finished row is merged with this partial result of the
@@ -163,7 +170,7 @@ __device__ __forceinline__ bool is_verify(int mode) {
 
 __device__ __forceinline__ int prefix_len(const AttnParams& p, int b) {
     int L = __ldg(p.lens + b);
-    return L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
+    return (L < 0 ? 0 : (L > p.max_len ? p.max_len : L)) + p.s_len;
 }
 
 __device__ __forceinline__ void prefill_keys(const AttnParams& p, int p0, int ntok, int& lo,
@@ -678,7 +685,10 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 const int key_base = x.tile_base * kBN;
                 auto load_page = [&](int box) -> int {
                     const int pos = key_base + box * p.boxr;
-                    return pos < x.valid_end ? __ldg(x.trow + pos / p.P) : -1;
+                    if (pos >= x.valid_end) return -1;
+                    if (pos < p.s_len)  // the group's shared prefix
+                        return __ldg(p.stab + (size_t)(x.b / p.s_grp) * p.stab_stride + pos / p.P);
+                    return __ldg(x.trow + (pos - p.s_len) / p.P);
                 };
                 int wbase = jb * NB;
                 int cur = load_page(wbase + lane);

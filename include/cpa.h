@@ -271,9 +271,9 @@ cpa_status cpa_prefill_hit(const void* q, const void* k_pages, const void* v_pag
 
 /*
  * Bytes of workspace cpa_cascade_verify_shared needs for these sizes on the
- * current device (0 for sizes it would reject).  Besides the status word and
- * merge scratch it holds two fp32 partial results, 2*B*topk*S*H_q*
- * (head_dim + 1) floats.
+ * current device (0 for sizes it would reject), for either of its schedules.
+ * Besides the status word and merge scratch it holds the first level's fp32
+ * partial result, B*topk*S*H_q*(head_dim + 1) floats.
  */
 size_t cpa_cascade_verify_shared_workspace_size(int B, int n_groups, int topk, int S, int H_q,
                                                 int H_kv, int head_dim, int page_size);
@@ -286,12 +286,18 @@ size_t cpa_cascade_verify_shared_workspace_size(int B, int n_groups, int topk, i
  * B/n_groups consecutive requests; each group has one shared prefix of
  * shared_len tokens, each request then its own prefix, each branch its own
  * drafts.  Draft s of branch k of request b sees the group's shared prefix,
- * request b's own prefix and drafts 0..s of branch k.  Three levels, merged
- * by the cascade page's log-sum-exp identity: the shared prefix is read once
- * per group for all the group's draft queries (the tensor-core kernel in its
- * rectangle mode, the group's queries as one block of suffix queries), the
- * own prefix once per request and the drafts once per branch (the fused
- * cascade kernel), then one merge.
+ * request b's own prefix and drafts 0..s of branch k.  The shared prefix is
+ * read from memory once per group:
+ *   - shared_len a multiple of page_size: one launch of the fused cascade
+ *     kernel; each request's prefix walk covers the group's shared pages and
+ *     then its own, and the requests of a group, scheduled together, take the
+ *     shared pages from L2 after the first read.
+ *   - otherwise three levels merged by the cascade page's log-sum-exp
+ *     identity: the shared prefix for all the group's draft queries at once
+ *     (the tensor-core kernel in its rectangle mode, the group's queries as one
+ *     block of suffix queries), then the own prefix once per request and the
+ *     drafts once per branch (the fused cascade kernel), which merges.
+ * Both give the same result up to rounding.
  *   shared_page_table  int32 [n_groups, shared_pt_stride]: the group's shared
  *                      pages; shared_pt_stride >= ceil(shared_len/page_size).
  *                      May be NULL when shared_len is 0.

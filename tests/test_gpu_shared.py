@@ -45,7 +45,22 @@ SMALL_SHARED = {
                            page_size=64, prefix_lens=[200, 1500, 0, 64], seed=83),
     "no_shared": dict(B=4, n_groups=2, shared_len=0, topk=3, S=2, H_q=8, H_kv=2, page_size=16,
                       prefix_lens=[100, 17, 0, 64], seed=84),
+    # whole shared pages (one launch) with two M tiles, groups of two requests
+    "paged_two_mtiles": dict(B=6, n_groups=3, shared_len=640, topk=8, S=4, H_q=64, H_kv=8,
+                             page_size=64, prefix_lens=[0, 1000, 64, 333, 1, 700], seed=85),
+    # whole shared pages, ragged own prefixes, one M tile, GQA 4
+    "paged_ragged_own": dict(B=6, n_groups=2, shared_len=128, topk=3, S=4, H_q=16, H_kv=4,
+                             page_size=16, prefix_lens=[5, 0, 250, 127, 128, 1], seed=86),
 }
+
+
+def test_shared_paths_cover_both_schedules():
+    """Whole shared pages take the one-launch schedule, a shared prefix that
+    ends inside a page the two-launch one: both are among the cases above."""
+    aligned = [k for k, c in SMALL_SHARED.items()
+               if c["shared_len"] > 0 and c["shared_len"] % c["page_size"] == 0]
+    ragged = [k for k, c in SMALL_SHARED.items() if c["shared_len"] % c["page_size"] != 0]
+    assert len(aligned) >= 2 and len(ragged) >= 2
 
 
 @pytest.mark.parametrize("key", list(SMALL_SHARED))
