@@ -743,7 +743,7 @@ cpa_status cpa_tree_verify(const void* q, const void* k_pages, const void* v_pag
                            int H_q, int H_kv, int head_dim, int page_size, int num_pages,
                            int max_prefix_len, float sm_scale, void* o, float* lse,
                            void* workspace, size_t workspace_bytes, cpa_stream_t stream) {
-    // everything checkable is checked before the mask kernel launches
+    // everything checkable is checked before the launch
     cpa_status st = check_verify(q, k_pages, v_pages, prefix_page_table, prefix_pt_stride,
                                  prefix_lens, B, 1, N, H_q, H_kv, head_dim, page_size, num_pages,
                                  max_prefix_len, sm_scale);

@@ -39,12 +39,13 @@
  *     DEVICE pointers (16-byte aligned for q, k_pages, v_pages, o) unless a
  *     comment says host.  The caller owns every buffer, including the
  *     workspace; the library never allocates, frees or synchronises (except
- *     cpa_get_device_status and cpa_noalloc_device_status, which say so).  Calls are asynchronous on
- *     `stream` (NULL = legacy default stream) and launch nothing when they
- *     return an error, with one exception: cpa_tree_verify and
- *     cpa_cascade_verify_shared launch more than one kernel, and check every
- *     argument before the first, so only CPA_ERR_LAUNCH or CPA_ERR_CUDA from
- *     a later launch can follow launches already made.
+ *     cpa_get_device_status and cpa_noalloc_device_status, which say so).
+ *     Calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *     launch nothing when they return an error, with one exception:
+ *     cpa_cascade_verify_shared launches two kernels when its shared prefix
+ *     ends inside a page, and checks every argument before the first, so only
+ *     CPA_ERR_LAUNCH or CPA_ERR_CUDA from the second launch can follow a
+ *     launch already made.
  *   - Errors: arguments that can be checked on the host return a status
  *     before any launch.  Problems only the GPU can see (a page id outside
  *     [0, num_pages), a prefix length outside [0, max_prefix_len], a pipeline
