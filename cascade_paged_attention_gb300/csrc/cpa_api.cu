@@ -854,9 +854,15 @@ int cpa_plan_partition(int64_t total, int n_ctas, int cta, int64_t tile, int64_t
     if (total < 1 || n_ctas < 1 || n_ctas > total || cta < 0 || cta >= n_ctas || tile < 0 ||
         tile >= total)
         return -1;
-    if (begin) *begin = split_begin(total, n_ctas, cta);
-    if (end) *end = split_begin(total, n_ctas, cta + 1);
-    return split_owner(total, n_ctas, tile);
+    const int64_t b = split_begin(total, n_ctas, cta), e = split_begin(total, n_ctas, cta + 1);
+    const int owner = split_owner(total, n_ctas, tile);
+    // the 32-bit form some kernel instances use must agree with the 64-bit one
+    if (b != split_begin(total, n_ctas, cta, true) || e != split_begin(total, n_ctas, cta + 1, true) ||
+        owner != split_owner(total, n_ctas, tile, true))
+        return -2;
+    if (begin) *begin = b;
+    if (end) *end = e;
+    return owner;
 }
 
 }  // extern "C"

@@ -121,8 +121,11 @@ struct AttnParams {
     const float* mrg_lse;
     uint32_t* status;
     uint32_t* counters;
-    float* part_o;    // [2*n_ctas][kMaxUnitRows][128]
-    float* part_lse;  // [2*n_ctas][kMaxUnitRows], log2 units
+    // split-unit parts, one slot per (CTA, first or last piece): o as 32 float4
+    // column groups of NUM_MT*128 rows each (a slot's part is contiguous), lse
+    // in log2 units; slots are kMaxUnitRows rows apart
+    float* part_o;    // [2*n_ctas][32][kMaxUnitRows] float4
+    float* part_lse;  // [2*n_ctas][kMaxUnitRows]
     int mode;
     int B, topk, S, H_q, H_kv, G, P, num_pages;
     int ptab_stride, dtab_stride, max_len;
@@ -358,6 +361,7 @@ __device__ __forceinline__ long long block_scan(long long v, long long* ws, long
 
 // Every thread of the CTA: find the problem's total tile count and where this
 // CTA's range begins.
+template <bool FAST32>
 __device__ __forceinline__ void schedule(const AttnParams& p, Ctrl* c) {
     long long total = 0;
     const int nthr = blockDim.x;
@@ -419,8 +423,8 @@ __device__ __forceinline__ void schedule(const AttnParams& p, Ctrl* c) {
         c->n_ctas = n_ctas;
         c->found = 0;
         if (cta < n_ctas) {
-            c->begin = split_begin(total, n_ctas, cta);
-            c->count = split_begin(total, n_ctas, cta + 1) - c->begin;
+            c->begin = split_begin(total, n_ctas, cta, FAST32);
+            c->count = split_begin(total, n_ctas, cta + 1, FAST32) - c->begin;
         } else {
             c->begin = 0;
             c->count = 0;
@@ -550,8 +554,12 @@ template <int NUM_MT, int VAR>
 __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     paged_attn_kernel(const __grid_constant__ AttnParams p) {
     using C = Cfg<NUM_MT>;
+    constexpr int kPartRows = NUM_MT * 128;  // rows of a split-unit part (see part_o)
     constexpr bool FP8 = VAR == VAR_FP8;
     constexpr bool TREE = VAR == VAR_TREE;
+    // 32-bit division in the work split: faster in every instance but the tree
+    // one, which measured 112.7 us without it against 117.4 us with it
+    constexpr bool kFast32 = !TREE;
     constexpr bool MERGE = VAR == VAR_MERGE;
 #ifdef CPA_TRACE
     unsigned long long* const cpa_trace_local = cpa_trace_buf;  // read once
@@ -616,7 +624,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    schedule(p, ctrl);
+    schedule<kFast32>(p, ctrl);
 #ifdef CPA_TRACE
     if (threadIdx.x == 0 && cpa_trace_local) {
         if (blockIdx.x < 4) {
@@ -1587,16 +1595,15 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     // stored is that last one and takes its own part straight from TMEM;
                     // otherwise it stores its part (O / l and its log-sum-exp) and counts
                     // itself in, and the piece that completes the count merges.
-                    const int c_first = split_owner(total, n_ctas, w.ustart);
-                    const int c_last = split_owner(total, n_ctas, w.ustart + x.n_tiles - 1);
+                    const int c_first = split_owner(total, n_ctas, w.ustart, kFast32);
+                    const int c_last = split_owner(total, n_ctas, w.ustart + x.n_tiles - 1, kFast32);
                     const int np = c_last - c_first + 1;
                     const int own = (int)blockIdx.x - c_first;
                     // (only as the CTA's final piece: a merge holds O in TMEM, and any
                     // later unit of this CTA waits for it)
                     const bool final_piece = w.left == (long long)(je - jb);
                     if (et == 0) {
-                        const unsigned seen =
-                            final_piece ? atomicAdd(p.counters + w.u, 0u) : 0u;
+                        const unsigned seen = final_piece ? ld_acquire_gpu(p.counters + w.u) : 0u;
                         ctrl->flag = (final_piece && seen == (unsigned)(np - 1)) ? 2 : 0;
                     }
                     named_bar_sync(1, 128);
@@ -1605,7 +1612,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         // the part stays in L2 until the merging CTA reads it, typically
                         // at the very end, after the whole K/V stream has passed through
                         const uint64_t pol_keep = l2_policy_evict_last();
-                        const int slot = split_slot(total, n_ctas, blockIdx.x, w.ustart);
+                        const int slot = split_slot(total, n_ctas, blockIdx.x, w.ustart, kFast32);
                         for (int mt = 0; mt < NUM_MT; ++mt) {
                             const int R = mt * 128 + r;
                             const float2 st = stats[R];
@@ -1625,7 +1632,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                 if (valid) {
 #pragma unroll
                                     for (int e = 0; e < 8; ++e)
-                                        st_global_hint(po + (blk * 8 + e) * kMaxUnitRows,
+                                        st_global_hint(po + (blk * 8 + e) * kPartRows,
                                                        make_float4(__uint_as_float(v[4 * e]) * inv,
                                                                    __uint_as_float(v[4 * e + 1]) * inv,
                                                                    __uint_as_float(v[4 * e + 2]) * inv,
@@ -1653,13 +1660,13 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     if (mode != 0) {
                         // mode 2: this piece's part comes from TMEM, the others' from memory.
                         // As the CTA's final piece every K/V stage is idle (all MMAs are
-                        // done): the other parts are bulk-copied there, one copy per float4
-                        // column group with the unit's rows side by side, so that the merge
-                        // waits on memory once instead of once per group and part.
-                        __threadfence();
-                        const int nrows = x.ntok * G;
-                        const int nl = (nrows + 3) & ~3;  // log-sum-exp entries copied per part
-                        const uint32_t part_bytes = 32u * (uint32_t)nrows * 16u;
+                        // done): each other part is bulk-copied there whole (one copy of
+                        // its contiguous slot), so that the merge waits on memory once.
+                        // (mode 1 counted itself in with a relaxed atomic: fence before
+                        // reading the others' parts; mode 2 read the count with acquire)
+                        if (mode == 1) __threadfence();
+                        const int nl = kPartRows;  // log-sum-exp entries copied per part
+                        const uint32_t part_bytes = 32u * (uint32_t)kPartRows * 16u;
                         const uint32_t lse_off = (uint32_t)(np - 1) * part_bytes;
                         const bool staged = mode == 2 && lse_off + (uint32_t)(np - 1) * nl * 4u <=
                                                              (uint32_t)p.n_stages * kStageBytes;
@@ -1667,26 +1674,25 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         const float* stage_lse = reinterpret_cast<const float*>(smem + p.off_kv + lse_off);
                         if (staged) {
                             if (et < 32) {
-                                // lane q of the first epilogue warp copies column group q of
-                                // every other part (one thread's copies issue one by one)
+                                // lane k of the first epilogue warp copies the k-th other part
+                                // and its log-sum-exp entries
                                 fence_proxy_async_global();
                                 if (et == 0)
                                     mbar_arrive_expect_tx(&ctrl->merge_full,
                                                           lse_off + (uint32_t)(np - 1) * nl * 4u);
                                 __syncwarp();
-                                for (int c = 0, k = 0; c < np; ++c) {
-                                    if (c == own) continue;
-                                    const size_t sl = split_slot(total, n_ctas, c_first + c, w.ustart);
-                                    const float4* src =
-                                        reinterpret_cast<const float4*>(p.part_o) + sl * 32 * kMaxUnitRows;
-                                    bulk_load(smem + p.off_kv + ((size_t)k * 32 + et) * nrows * 16,
-                                              src + (size_t)et * kMaxUnitRows, (uint32_t)nrows * 16u,
+                                const int k = et;
+                                if (k < np - 1) {
+                                    const int c = k < own ? k : k + 1;
+                                    const size_t sl =
+                                        split_slot(total, n_ctas, c_first + c, w.ustart, kFast32);
+                                    bulk_load(smem + p.off_kv + (size_t)k * part_bytes,
+                                              reinterpret_cast<const float4*>(p.part_o) +
+                                                  sl * 32 * kMaxUnitRows,
+                                              part_bytes, &ctrl->merge_full);
+                                    bulk_load(smem + p.off_kv + lse_off + (size_t)k * nl * 4,
+                                              p.part_lse + sl * kMaxUnitRows, (uint32_t)nl * 4u,
                                               &ctrl->merge_full);
-                                    if (et == 0)
-                                        bulk_load(smem + p.off_kv + lse_off + (size_t)k * nl * 4,
-                                                  p.part_lse + sl * kMaxUnitRows, (uint32_t)nl * 4u,
-                                                  &ctrl->merge_full);
-                                    ++k;
                                 }
                             }
                             // at most one staged merge per CTA: phase 0
@@ -1706,7 +1712,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                             const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
                             const uint32_t oaddr = tmem + lane_addr + C::o_col(mt);
                             auto slot_of = [&](int c) -> size_t {
-                                return (size_t)split_slot(total, n_ctas, c_first + c, w.ustart);
+                                return (size_t)split_slot(total, n_ctas, c_first + c, w.ustart, kFast32);
                             };
                             auto lse_of = [&](int c) -> float {
                                 if (mode == 2 && c == own) return lse_own;
@@ -1747,14 +1753,15 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                                     float4 v4[8];
                                     if (staged) {
                                         const float4* s4 =
-                                            stage4 + ((size_t)(c < own ? c : c - 1) * 32 + blk * 8) * nrows + R;
+                                            stage4 + ((size_t)(c < own ? c : c - 1) * 32 + blk * 8) * kPartRows + R;
 #pragma unroll
-                                        for (int e = 0; e < 8; ++e) v4[e] = s4[e * nrows];
+                                        for (int e = 0; e < 8; ++e) v4[e] = s4[e * kPartRows];
                                     } else {
                                         const float4* s4 = reinterpret_cast<const float4*>(p.part_o) +
-                                                           (slot_of(c) * 32 + blk * 8) * kMaxUnitRows + R;
+                                                           slot_of(c) * 32 * kMaxUnitRows +
+                                                           (size_t)blk * 8 * kPartRows + R;
 #pragma unroll
-                                        for (int e = 0; e < 8; ++e) v4[e] = __ldcg(s4 + e * kMaxUnitRows);
+                                        for (int e = 0; e < 8; ++e) v4[e] = __ldcg(s4 + e * kPartRows);
                                     }
 #pragma unroll
                                     for (int e = 0; e < 8; ++e) {

@@ -32,11 +32,20 @@ enum Mode : int {
 
 // Balanced contiguous split of `total` tiles over `n` CTAs:
 // CTA c owns tiles [floor(c*T/n), floor((c+1)*T/n)).
-CPA_HD int64_t split_begin(int64_t total, int n, int c) { return (total * c) / n; }
+// With fast32, a 32-bit division whenever total * n fits (a 64-bit division
+// is a long software sequence on the GPU).  Both give the same result; the
+// kernel instances choose the form that measured faster for them.
+CPA_HD int64_t split_begin(int64_t total, int n, int c, bool fast32 = false) {
+    if (fast32 && (uint64_t)total * (uint64_t)n < 0x80000000ull)
+        return (int64_t)((uint32_t)total * (uint32_t)c / (uint32_t)n);
+    return (total * c) / n;
+}
 
 // The CTA whose range holds tile x: the largest c with floor(c*T/n) <= x,
 // which is ceil((x+1)*n/T) - 1.
-CPA_HD int split_owner(int64_t total, int n, int64_t x) {
+CPA_HD int split_owner(int64_t total, int n, int64_t x, bool fast32 = false) {
+    if (fast32 && (uint64_t)total * (uint64_t)n < 0x80000000ull)
+        return (int)(((uint32_t)(x + 1) * (uint32_t)n - 1u) / (uint32_t)total);
     return (int)(((x + 1) * (int64_t)n - 1) / total);
 }
 
@@ -44,8 +53,8 @@ CPA_HD int split_owner(int64_t total, int n, int64_t x) {
 // u_start: slot 2c if that piece is the CTA's first piece of work, 2c+1 if
 // the CTA began inside an earlier unit.  Only a CTA's first and last pieces
 // can be split, so two slots per CTA suffice.
-CPA_HD int split_slot(int64_t total, int n, int c, int64_t u_start) {
-    return 2 * c + ((split_begin(total, n, c) < u_start) ? 1 : 0);
+CPA_HD int split_slot(int64_t total, int n, int c, int64_t u_start, bool fast32 = false) {
+    return 2 * c + ((split_begin(total, n, c, fast32) < u_start) ? 1 : 0);
 }
 
 }  // namespace cpa

@@ -404,7 +404,9 @@ cpa_status cpa_debug_wait_timeout(void* workspace, size_t workspace_bytes, int l
  * Host-side view of the work partition the attention kernels use, for
  * tests: `total` tiles split over `n_ctas` CTAs, CTA c owning
  * [begin, end).  Returns the owner CTA of tile `tile` and fills begin/end
- * of CTA `cta` (host pointers).  Returns -1 on bad arguments.
+ * of CTA `cta` (host pointers).  Returns -1 on bad arguments, and -2 if the
+ * two forms of the split arithmetic the kernels use (64-bit division, and
+ * 32-bit division where total * n_ctas < 2^31) disagree, which they must not.
  */
 int cpa_plan_partition(int64_t total, int n_ctas, int cta, int64_t tile, int64_t* begin,
                        int64_t* end);

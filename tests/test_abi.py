@@ -142,6 +142,23 @@ def test_partition_covers_every_tile_once(L, total, n):
         assert b <= t < e
 
 
+def test_partition_split_arithmetic_forms_agree(L):
+    """The 32-bit form of the split arithmetic (used where total * n < 2^31) gives the
+    64-bit form's begin, end and owner: every CTA boundary and its neighbours, for sizes
+    up to the 2^31 limit."""
+    rng = np.random.default_rng(11)
+    cases = [(16384, 152), (2 ** 31 // 152 - 1, 152), (2 ** 31 // 152 + 1, 152), (1, 1),
+             (8704, 152), (2 ** 31 // 7 - 3, 7)]
+    cases += [(int(rng.integers(1, 2 ** 24)), int(rng.integers(1, 300))) for _ in range(40)]
+    for total, n in cases:
+        n = min(n, total)
+        for c in sorted({0, n - 1, n // 2, int(rng.integers(0, n))}):
+            r = cpa.cpa_plan_partition(total, n, c, 0)
+            assert r[0] >= 0, (total, n, c)
+            for t in {r[1], r[2] - 1, max(r[1] - 1, 0), min(r[2], total - 1)}:
+                assert cpa.cpa_plan_partition(total, n, c, int(t))[0] >= 0, (total, n, t)
+
+
 def test_partition_split_units_are_merged_once(L):
     """Every unit split over CTAs is owned by a contiguous CTA run, each with a nonempty piece,
     and the two partial slots per CTA never collide."""
