@@ -240,6 +240,8 @@ cpa_status run_attn(AttnParams& p, const Geometry& geo, long long n_units, void*
         e = launch_attn_mt<VAR_TREE>(p, geo, n_sm, stream);
     else if (p.mrg_o)
         e = launch_attn_mt<VAR_MERGE>(p, geo, n_sm, stream);
+    else if ((p.mode == MODE_PREFILL || p.mode == MODE_PREFILL_TRI) && geo.num_mt == 1)
+        e = launch_attn<1, VAR_PREFILL>(p, geo.smem_bytes, n_sm, stream);
     else
         e = launch_attn_mt<VAR_PLAIN>(p, geo, n_sm, stream);
     return e == cudaSuccess ? CPA_OK : CPA_ERR_LAUNCH;

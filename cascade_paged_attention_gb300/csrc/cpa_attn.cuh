@@ -548,6 +548,8 @@ enum Variant : int {
                     // masked per row by ancestor masks
     VAR_MERGE = 3,  // bf16 pools; every finished row is merged with another
                     // launch's partial result (p.mrg_o) before it is written
+    VAR_PREFILL = 4,  // prefill (full or triangle): units are never split and
+                      // have no draft tile, so neither path is compiled in
 };
 
 template <int NUM_MT, int VAR>
@@ -561,6 +563,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
     // one, which measured 112.7 us without it against 117.4 us with it
     constexpr bool kFast32 = !TREE;
     constexpr bool MERGE = VAR == VAR_MERGE;
+    constexpr bool PREFILL = VAR == VAR_PREFILL;
 #ifdef CPA_TRACE
     unsigned long long* const cpa_trace_local = cpa_trace_buf;  // read once
 #endif
@@ -748,7 +751,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         }
                         continue;
                     }
-                    if (jj >= x.n_prefix) {
+                    if (!PREFILL && jj >= x.n_prefix) {
                         // the unit's draft tile: branch k's drafts 0..S-1 sit in slots
                         // 0..S-1 of its first draft page; copy t = 4k + part loads one
                         // sb-row box (K lo/hi, V lo/hi) into rows k*sb.. of the tile
@@ -1156,7 +1159,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                     bool okl = mbar_wait_warp(&ctrl->s_full[bi], par, abort_flag, p.status);
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(4, g);
                     if (lane == 0) CPA_TRACE_EVENT(20 + warp - C::kSmWarp0, g);
-                    const bool dtile = jj >= x.n_prefix;
+                    const bool dtile = !PREFILL && jj >= x.n_prefix;
                     const bool tree_tile = TREE && dtile;
                     const int key0 = (x.tile_base + jj) * kBN;
                     // visible columns [lo_c, hi_c) of this tile for this row
@@ -1491,7 +1494,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                 const Unit x = get_unit(p, w.u);
                 int jb, je;
                 w.piece(x, jb, je);
-                const bool split = jb > 0 || je < x.n_tiles;
+                const bool split = !PREFILL && (jb > 0 || je < x.n_tiles);
                 const uint32_t ph = (uint32_t)(w.seg & 1);
                 ok = mbar_wait(&ctrl->o_full, ph, abort_flag, p.status) &&
                      mbar_wait(&ctrl->stats_full, ph, abort_flag, p.status);
