@@ -1292,15 +1292,19 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                         // 16k..16k+15 of the chunk (S there is already read).  (The MMA that
                         // produced S is done, and so is every earlier MMA: no PV still reads
                         // these columns.)
-                        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                        // (scores scaled and the sum kept two at a time: one packed f32x2
+                        // FMA and one packed add per pair of columns)
+                        float2 s2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                        const float2 nm2 = make_float2(-mref, -mref);
                         auto exp_piece = [&](const uint32_t (&sv)[32], uint32_t (&pk)[16]) {
 #pragma unroll
                             for (int c = 0; c < 16; ++c) {
-                                const float ea =
-                                    ex2(fmaf(__uint_as_float(sv[2 * c]), p.scale_log2, -mref));
-                                const float eb =
-                                    ex2(fmaf(__uint_as_float(sv[2 * c + 1]), p.scale_log2, -mref));
-                                s4[c & 3] += ea + eb;
+                                const float2 t = __ffma2_rn(make_float2(__uint_as_float(sv[2 * c]),
+                                                                        __uint_as_float(sv[2 * c + 1])),
+                                                            sc2, nm2);
+                                const float ea = ex2(t.x), eb = ex2(t.y);
+                                s2[c & 1] = __fadd2_rn(s2[c & 1], make_float2(ea, eb));
                                 pk[c] = FP8 ? pack_f16x2(ea, eb) : pack_bf16x2(ea, eb);
                             }
                         };
@@ -1365,7 +1369,7 @@ __global__ void __launch_bounds__(Cfg<NUM_MT>::kThreads, 1)
                             }
                         }
                         tmem_wait_st();
-                        l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                        l += (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y);
                     }
                     if (threadIdx.x == C::kSmWarp0 * 32) CPA_TRACE_EVENT(5, g);
                     if (lane == 0) CPA_TRACE_EVENT(44 + warp - C::kSmWarp0, g);
