@@ -39,6 +39,11 @@ SMALL_VERIFY = {
                       prefix_lens=[200, 1000], seed=36),
     "topk8_s12_two_mtiles": dict(B=2, topk=8, S=12, H_q=16, H_kv=8, page_size=16,
                                  prefix_lens=[300, 40], seed=37),
+    # 64 units of 17 tiles over about 7 tiles per CTA (152 SMs): units split over
+    # three or four CTAs, so the final merges take two or three other parts, the
+    # staged (one bulk copy per part) and the unstaged forms
+    "split3": dict(B=8, topk=4, S=5, H_q=32, H_kv=8, page_size=16,
+                   prefix_lens=[2000, 1999, 2000, 1873, 2000, 2000, 1024, 2000], seed=38),
 }
 
 
