@@ -49,6 +49,18 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def recorded_traffic(path: str, current_hash: str):
+    """DRAM bytes per launch from a committed capture summary, or None when the
+    file is missing or was taken on other kernel sources (its hash differs)."""
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        prof = json.load(f)
+    if prof.get("kernel_hash") != current_hash:
+        return None
+    return prof.get("dram_bytes_per_launch")
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -553,12 +565,7 @@ def run_ours(args, world, rank, local):
 
     peak, peak_kind = measured_peaks()
     peak_tf = measured_bf16_tflops()
-    traffic = None
-    if os.path.exists(PROFILE_SUMMARY):
-        with open(PROFILE_SUMMARY) as f:
-            prof = json.load(f)
-        if prof.get("kernel_hash") == kernel_hash():
-            traffic = prof.get("dram_bytes_per_launch")
+    traffic = recorded_traffic(PROFILE_SUMMARY, kernel_hash())
 
     do_cpu = rank == 0 and not args.no_cpu_baseline
     configs = []
